@@ -1,0 +1,387 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+* the cache-statistics example the pages print (golden fixture);
+* closed forms of the visible set (patch pages, special tokens, last page length);
+* bookkeeping invariants (page conservation, no duplicate ids, specials never leave);
+* brute force: dense attention over the whole frame history, sliced by the window
+  rules, computed with float64 scaled_dot_product_attention from PyTorch;
+* invariance under permutation of physical page ids;
+* closed forms of attention (equal keys, one dominant key, V scaling, key shift);
+* the log-sum-exp merge equals attention over the union, and lse equals a library
+  logsumexp of the logits;
+* planted mistakes in the oracle are caught by at least one of the pins above.
+"""
+from __future__ import annotations
+
+import contextlib
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+import oracle.attention as oatt
+import oracle.paged_cache as opc
+import workloads as wl
+from oracle_cases import make_streams, step
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _small(**kw):
+    base = dict(name="small", num_blocks=1, num_streams=1, num_heads=2, head_dim=16, page_size=8,
+                patches_per_frame=8, specials_per_frame=3, scale_frames=2, sliding_window=3,
+                frames=12, dtype="f32", value_scale=1.0)
+    base.update(kw)
+    return wl.Workload(**base)
+
+
+SMALL_VARIANTS = [
+    _small(),
+    _small(page_size=16, patches_per_frame=11, specials_per_frame=5),   # pad slots on patch pages
+    _small(page_size=4, patches_per_frame=4, specials_per_frame=6),     # specials straddle 2+ pages
+    _small(scale_frames=0, sliding_window=1),
+    _small(scale_frames=0, sliding_window=0),                            # specials only
+    _small(scale_frames=5, sliding_window=0, frames=9),
+    _small(num_streams=2, shuffle_pages=True, frames=10),
+    _small(num_heads=3, head_dim=8, frames=7, specials_per_frame=1, page_size=2, patches_per_frame=2),
+]
+
+
+# ---------------------------------------------------------------- pin helpers
+
+def pin_golden_stats():
+    with open(os.path.join(GOLDEN, "cache_stats_after_42_frames.json")) as fh:
+        g = json.load(fh)
+    s = g["setup"]
+    st = oracle.StreamPages(patches_per_frame=s["patches_per_frame"], specials_per_frame=s["specials_per_frame"],
+                            page_size=s["page_size"], scale_frames=s["scale_frames"],
+                            sliding_window=s["sliding_window"],
+                            patch_ids=range(s["max_patch_pages"]),
+                            special_ids=range(s["max_patch_pages"], s["max_patch_pages"] + s["max_special_pages"]))
+    for _ in range(s["frames"]):
+        st.append()
+        st.evict()
+    assert st.stats() == g["expected"], st.stats()
+
+
+def closed_form(cfg, f):
+    sc, w, P, S, ps = cfg.scale_frames, cfg.sliding_window, cfg.patches_per_frame, cfg.specials_per_frame, cfg.page_size
+    n_patch = min(f, sc) + min(max(f - sc, 0), w)
+    st = f * S
+    ns = -(-st // ps)
+    lpl = st - (ns - 1) * ps
+    return n_patch, st, ns, lpl, n_patch * P + st
+
+
+def pin_closed_forms(cfg, frames=None, check_sources_every=1):
+    streams = make_streams(cfg)
+    frames = cfg.frames if frames is None else frames
+    seen_special = [[] for _ in streams]
+    for f in range(1, frames + 1):
+        step(streams)
+        n_patch, st_tok, ns, lpl, n_vis = closed_form(cfg, f)
+        p = oracle.plan(streams, cfg.tokens_per_frame)
+        for s, st in enumerate(streams):
+            assert p["num_patch_pages"][s] == n_patch
+            assert st.special_tokens == st_tok
+            assert len(st.special_pages) == ns
+            assert p["last_page_len"][s] == lpl and 1 <= lpl <= cfg.page_size
+            assert p["kv_indptr"][s + 1] - p["kv_indptr"][s] == n_patch + ns
+            # invariants: page conservation, no duplicates, specials only grow
+            assert len(st.free) + len(st.scale) + len(st.live) == cfg.max_patch_pages
+            ids = list(st.free) + st.scale + list(st.live)
+            assert len(set(ids)) == len(ids)
+            assert st.special_pages[:len(seen_special[s])] == seen_special[s]
+            seen_special[s] = list(st.special_pages)
+            if f % check_sources_every == 0:
+                assert len(st.visible_sources()) == n_vis
+        assert p["qo_indptr"] == [i * cfg.tokens_per_frame for i in range(len(streams) + 1)]
+
+
+def history_keys(cfg, hist_k, hist_v, f):
+    """Brute-force visible set from the dense history: window rules applied to frames."""
+    sc, w, P = cfg.scale_frames, cfg.sliding_window, cfg.patches_per_frame
+    patch_frames = list(range(min(f, sc))) + list(range(max(sc, f - w), f))
+    k = [hist_k[i][:P] for i in patch_frames] + [hist_k[i][P:] for i in range(f)]
+    v = [hist_v[i][:P] for i in patch_frames] + [hist_v[i][P:] for i in range(f)]
+    return np.concatenate(k), np.concatenate(v)
+
+
+def sdpa64(q, k, v):
+    """float64 scaled_dot_product_attention from PyTorch: q [T,H,D], k/v [N,H,D]."""
+    qt = torch.from_numpy(np.ascontiguousarray(q.transpose(1, 0, 2)))[None]
+    kt = torch.from_numpy(np.ascontiguousarray(k.transpose(1, 0, 2)))[None]
+    vt = torch.from_numpy(np.ascontiguousarray(v.transpose(1, 0, 2)))[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)
+    return o[0].numpy().transpose(1, 0, 2)
+
+
+def pin_brute_force(cfg, seed=0):
+    rng = np.random.default_rng(seed)
+    T, H, D = cfg.tokens_per_frame, cfg.num_heads, cfg.head_dim
+    streams = make_streams(cfg)
+    hist = [([], []) for _ in streams]
+    stores = [dict() for _ in streams]
+    for f in range(1, cfg.frames + 1):
+        for s, st in enumerate(streams):
+            k = rng.standard_normal((T, H, D)); v = rng.standard_normal((T, H, D))
+            hist[s][0].append(k); hist[s][1].append(v)
+            stores[s][f - 1] = (k, v)
+        step(streams)
+        for s, st in enumerate(streams):
+            q = rng.standard_normal((T, H, D))
+            store = stores[s]
+            kv, vv = oracle.gather_visible(st.visible_sources(),
+                                           lambda fr, rows, store=store: (store[fr][0][rows], store[fr][1][rows]))
+            o, _ = oracle.attend(q, kv, vv)
+            kb, vb = history_keys(cfg, hist[s][0], hist[s][1], f)
+            ref = sdpa64(q, kb, vb)
+            np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+
+
+def pin_permutation(seed=1):
+    base = _small(frames=11, page_size=4, patches_per_frame=3, specials_per_frame=3, num_streams=2)
+    perm = base.replace(shuffle_pages=True)
+    rng = np.random.default_rng(seed)
+    T, H, D = base.tokens_per_frame, base.num_heads, base.head_dim
+    sa, sb = make_streams(base), make_streams(perm)
+    po, so = wl.page_orders(perm)
+    mpp, msp, B = base.max_patch_pages, base.max_special_pages, base.num_streams
+    # ascending id -> permuted id (k-th id of a stream's list maps to the k-th of the other)
+    idmap = {}
+    for s in range(B):
+        pa, spa = oracle.default_page_ids(B, mpp, msp, s)
+        idmap.update(zip(pa, po[s * mpp:(s + 1) * mpp].tolist()))
+        idmap.update(zip(spa, so[s * msp:(s + 1) * msp].tolist()))
+    store = [dict() for _ in range(B)]
+    for f in range(perm.frames):
+        for s in range(B):
+            store[s][f] = (rng.standard_normal((T, H, D)), rng.standard_normal((T, H, D)))
+        step(sa); step(sb)
+        pa_, pb_ = oracle.plan(sa, T), oracle.plan(sb, T)
+        assert pb_["indices"] == [idmap[i] for i in pa_["indices"]]
+        for key in ("kv_indptr", "last_page_len", "num_patch_pages", "qo_indptr"):
+            assert pa_[key] == pb_[key]
+        q = rng.standard_normal((T, H, D))
+        for s in range(B):
+            fetch = lambda fr, rows, s=s: (store[s][fr][0][rows], store[s][fr][1][rows])
+            oa, _ = oracle.attend(q, *oracle.gather_visible(sa[s].visible_sources(), fetch))
+            ob, _ = oracle.attend(q, *oracle.gather_visible(sb[s].visible_sources(), fetch))
+            np.testing.assert_allclose(oa, ob, rtol=0, atol=1e-12)
+
+
+def pin_attention_closed_forms(seed=2):
+    rng = np.random.default_rng(seed)
+    T, N, H, D = 5, 37, 3, 16
+    q = rng.standard_normal((T, H, D))
+    v = rng.standard_normal((N, H, D))
+    # equal keys -> mean of V
+    k = np.broadcast_to(rng.standard_normal((1, H, D)), (N, H, D)).copy()
+    o, lse = oracle.attend(q, k, v)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=0), (T, H, D)), atol=1e-12)
+    # lse of equal keys: logit + log N
+    logit = np.einsum("thd,hd->th", q, k[0]) / math.sqrt(D)
+    np.testing.assert_allclose(lse, logit + math.log(N), atol=1e-12)
+    # one dominant key -> its V row (keys small, one key along q_row with a huge logit)
+    k = 0.01 * rng.standard_normal((N, H, D))
+    j = 17
+    for h in range(H):
+        k[j, h] = 400.0 * q[0, h] / np.linalg.norm(q[0, h]) * math.sqrt(D) / np.linalg.norm(q[0, h])
+    o, _ = oracle.attend(q[:1], k, v)
+    np.testing.assert_allclose(o[0], v[j], atol=1e-9)
+    # random keys: V scaling and shifting every key by one vector (logit shift per row)
+    k = rng.standard_normal((N, H, D))
+    o, lse = oracle.attend(q, k, v)
+    o2, _ = oracle.attend(q, k, 3.5 * v)
+    np.testing.assert_allclose(o2, 3.5 * o, atol=1e-12)
+    u = rng.standard_normal((1, H, D))
+    o3, _ = oracle.attend(q, k + u, v)
+    np.testing.assert_allclose(o3, o, atol=1e-12)
+    # lse against a library logsumexp of the scaled logits
+    logits = np.einsum("thd,nhd->thn", q, k) / math.sqrt(D)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(logits, axis=2), atol=1e-12)
+    # single frame, no scale frames: plain self-attention (library routine)
+    np.testing.assert_allclose(o, sdpa64(q, k, v), atol=1e-12)
+
+
+def pin_merge(seed=3):
+    rng = np.random.default_rng(seed)
+    T, N, H, D = 7, 50, 2, 8
+    q, k, v = (rng.standard_normal(s) for s in ((T, H, D), (N, H, D), (N, H, D)))
+    full_o, full_l = oracle.attend(q, k, v)
+    for cuts in ([1], [25], [49], [3, 30], [10, 11, 40]):
+        edges = [0, *cuts, N]
+        parts = [oracle.attend(q, k[a:b], v[a:b]) for a, b in zip(edges[:-1], edges[1:])]
+        o, l = oracle.merge(parts)
+        np.testing.assert_allclose(o, full_o, atol=1e-12)
+        np.testing.assert_allclose(l, full_l, atol=1e-12)
+    o, l = oracle.merge([(full_o, full_l)])
+    np.testing.assert_allclose(o, full_o, atol=1e-14)
+
+
+PINS = {
+    "golden_stats": pin_golden_stats,
+    "closed_forms": lambda: [pin_closed_forms(c) for c in SMALL_VARIANTS],
+    "brute_force": lambda: [pin_brute_force(c, i) for i, c in enumerate(SMALL_VARIANTS)],
+    "permutation": pin_permutation,
+    "attention_closed_forms": pin_attention_closed_forms,
+    "merge": pin_merge,
+}
+
+
+# ---------------------------------------------------------------- tests
+
+def test_golden_stats_example():
+    pin_golden_stats()
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL_VARIANTS)))
+def test_closed_forms_small(idx):
+    pin_closed_forms(SMALL_VARIANTS[idx])
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_closed_forms_workloads(n):
+    cfg = wl.CONFIGS[n]
+    # every frame of every workload; the dense source list is checked on a stride
+    pin_closed_forms(cfg, check_sources_every=max(1, cfg.frames // 20))
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL_VARIANTS)))
+def test_brute_force_history(idx):
+    pin_brute_force(SMALL_VARIANTS[idx], idx)
+
+
+def test_brute_force_config1_shape():
+    pin_brute_force(wl.CONFIGS[1], 99)
+
+
+def test_permutation_invariance():
+    pin_permutation()
+
+
+def test_attention_closed_forms():
+    pin_attention_closed_forms()
+
+
+def test_lse_merge():
+    pin_merge()
+
+
+def test_append_failure_changes_nothing():
+    cfg = _small(frames=2)   # max_special_pages = ceil(2*3/8) = 1: the third frame needs a second page
+    st = make_streams(cfg)[0]
+    for _ in range(2):
+        st.append(); st.evict()
+    before = (list(st.free), list(st.scale), list(st.live), list(st.special_pages), st.special_tokens, st.frame_count)
+    with pytest.raises(oracle.OutOfSpecialPages):
+        st.append()
+    after = (list(st.free), list(st.scale), list(st.live), list(st.special_pages), st.special_tokens, st.frame_count)
+    assert before == after
+    cfg = _small(frames=40, scale_frames=2, sliding_window=3, headroom=0)
+    st = make_streams(cfg)[0]
+    for _ in range(5):
+        st.append()          # no eviction: 2 scale + 3 live fill all 5 patch pages
+    with pytest.raises(oracle.OutOfPatchPages):
+        st.append()
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+@contextlib.contextmanager
+def _patched(obj, name, value):
+    old = getattr(obj, name)
+    setattr(obj, name, value)
+    try:
+        yield
+    finally:
+        setattr(obj, name, old)
+
+
+def _evict_keep_one_less(self):
+    while len(self.live) > max(self.w - 1, 0):
+        self.free.append(self.live.popleft())
+
+
+def _evict_lifo(self):
+    while len(self.live) > self.w:
+        self.free.append(self.live.pop())
+
+
+def _evict_scale_too(self):
+    while len(self.live) > self.w:
+        self.free.append(self.live.popleft())
+    if len(self.scale) > 1 and self.frame_count > self.sc + self.w:
+        self.free.append(self.scale.pop(0))
+
+
+def _lpl_off_by_one(self):
+    n = len(self.special_pages)
+    return (self.special_tokens - (n - 1) * self.ps) % self.ps
+
+
+def _attend_no_scale(q, k, v):
+    return _ORIG_ATTEND(q * math.sqrt(q.shape[2]), k, v)
+
+
+def _attend_k_for_v(q, k, v):
+    return _ORIG_ATTEND(q, k, k)
+
+
+def _attend_causal_drop_last(q, k, v):
+    return _ORIG_ATTEND(q, k[:-1], v[:-1])
+
+
+def _merge_wrong_sign(parts):
+    lses = np.stack([l for _, l in parts]); outs = np.stack([o for o, _ in parts])
+    m = lses.max(axis=0); w = np.exp(m - lses); total = w.sum(axis=0)
+    return (w[..., None] * outs).sum(axis=0) / total[..., None], m + np.log(total)
+
+
+_ORIG_ATTEND = oatt.attend
+
+
+def _sources_skip_pad_wrong(self):
+    out = []
+    for pid in self.scale + list(self.live):
+        page = self.contents[pid]
+        out.extend(page[t] for t in range(self.P - 1))
+    n = len(self.special_pages)
+    for i, sp in enumerate(self.special_pages):
+        count = self.ps if i < n - 1 else self.last_page_len()
+        out.extend(self.contents[sp][t] for t in range(count))
+    return out
+
+
+MUTATIONS = {
+    "window_excludes_current_frame": (opc.StreamPages, "evict", _evict_keep_one_less),
+    "lifo_eviction": (opc.StreamPages, "evict", _evict_lifo),
+    "scale_pages_evicted": (opc.StreamPages, "evict", _evict_scale_too),
+    "last_page_len_zero_when_full": (opc.StreamPages, "last_page_len", _lpl_off_by_one),
+    "patch_page_short_by_one": (opc.StreamPages, "visible_sources", _sources_skip_pad_wrong),
+    "missing_softmax_scale": (oatt, "attend", _attend_no_scale),
+    "k_used_as_v": (oatt, "attend", _attend_k_for_v),
+    "last_key_dropped": (oatt, "attend", _attend_causal_drop_last),
+    "merge_weight_sign": (oatt, "merge", _merge_wrong_sign),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    obj, attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(obj, attr, fn)
+    # the package re-exports attend/merge: patch those too
+    if obj is oatt:
+        monkeypatch.setattr(oracle, attr, fn)
+    caught = []
+    for pin_name, pin in PINS.items():
+        try:
+            pin()
+        except (AssertionError, KeyError, IndexError, ValueError):
+            caught.append(pin_name)
+    assert caught, f"no pin caught the planted mistake {name}"
