@@ -1,0 +1,484 @@
+"""Throughput of streaming two-stream paged-KV attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl reference]
+
+A step is one frame-step of the whole hot path for one stream set: append of the
+frame's K/V for every block, one evict, one plan, and attention (+ merge) for every
+block.  The default workload is the 10,000-frame steady state (24 blocks, 16 heads
+of 64, 256 patch + 6 special tokens per frame, 8 scale frames, 64-frame window):
+the stream is fast-forwarded (append + evict for every block) to frame
+10000 - K - W, then W warm-up and K timed frame-steps run on device-resident
+inputs.  Visible K/V per block (~322 MB) exceeds L2, so no flush is needed between
+steps.
+
+Printed: one JSON line with the metric, a roofline object for the attention
+launch (algorithmic bytes per block / CUDA-event launch time, against the
+measured HBM copy bandwidth), an end-to-end figure through host buffers, the fp64
+oracle timed on the host cores (cpu_baseline) and the SM clocks sampled during the
+timed region.  With --gpus N > 1 (torchrun), every rank runs its own stream
+(weak scaling, no collective on the data path); the slowest rank's time counts.
+
+--impl reference times the fp64 CPU oracle itself (the only reference that
+exists for this path) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+for _p in (ROOT, os.path.join(ROOT, "tests")):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged-attn frame-steps/s (all blocks, 1 GB300); % of attention roofline"
+UNIT = "frame-steps/s"
+
+
+# ---------------------------------------------------------------- rank helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, world_size=world, rank=rank)
+    return world, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max of a scalar over ranks (timing only: no data-path collective)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(steps_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job frame-steps/s: every rank's steps over the slowest rank's time."""
+    return steps_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------- roofline helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def visible_tokens(w: wl.Workload, f: int) -> int:
+    """Visible keys per stream after f frames: (min(f,sc) + min(max(f-sc,0),w)) * P + f * S."""
+    sc, win, P, S = w.scale_frames, w.sliding_window, w.patches_per_frame, w.specials_per_frame
+    return (min(f, sc) + min(max(f - sc, 0), win)) * P + f * S
+
+
+def block_work(w: wl.Workload, f: int):
+    """Algorithmic FLOPs and bytes of one block's attention at frame f (all streams):
+    F = 4 T N H D B, bytes = (2N + 2T) H D e B (visible K+V once, q read, out written)."""
+    n = visible_tokens(w, f)
+    t, h, d, b, e = w.tokens_per_frame, w.num_heads, w.head_dim, w.num_streams, wl.element_bytes(w)
+    return 4.0 * t * n * h * d * b, (2.0 * n + 2.0 * t) * h * d * e * b
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.device_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0])); mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def oracle_block_sample(w: wl.Workload, frame_count: int, heads: int, reps: int, budget_s: float):
+    """Time the fp64 oracle (bookkeeping of one frame + gather + dense attention of one
+    block restricted to `heads` heads) at the steady state; returns per-rep seconds
+    and the extrapolated frame-steps/s."""
+    import oracle
+    from oracle_cases import make_streams
+
+    st = make_streams(w.replace(num_streams=1))[0]
+    for _ in range(frame_count - 1):
+        st.append(); st.evict()
+    hs = slice(0, heads)
+    # input generation is not timed: draw every frame a rep can see, once, head-sliced
+    P = w.patches_per_frame
+    last = frame_count + reps
+    patch_frames = set(range(min(last, w.scale_frames))) | set(range(max(0, frame_count - w.sliding_window - 1), last))
+    patch, special = {}, {}
+    for frame in sorted(patch_frames):
+        kp, vp = wl.frame_patch_kv(w, 0, 0, frame)
+        patch[frame] = (wl.to_f64(kp, w.dtype)[:, hs], wl.to_f64(vp, w.dtype)[:, hs])
+    for frame in range(last):
+        ks, vs = wl.frame_special_kv(w, 0, 0, frame)
+        special[frame] = (wl.to_f64(ks, w.dtype)[:, hs], wl.to_f64(vs, w.dtype)[:, hs])
+    q = wl.to_f64(wl.frame_q(w, 0, 0, frame_count - 1), w.dtype)[:, hs]
+
+    def fetch(frame, rows):
+        rows = np.asarray(rows)
+        if rows[0] < P:
+            k, v = patch[frame]
+            return k[rows], v[rows]
+        k, v = special[frame]
+        return k[rows - P], v[rows - P]
+
+    times = []
+    t_start = time.perf_counter()
+    for i in range(reps):
+        t0 = time.perf_counter()
+        st.append(); st.evict()
+        oracle.plan([st], w.tokens_per_frame)
+        k, v = oracle.gather_visible(st.visible_sources(), fetch)
+        oracle.attend(q, k, v)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    per_block = statistics.mean(times) * (w.num_heads / heads)
+    value = 1.0 / (per_block * w.num_blocks)
+    return times, value
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, w: wl.Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    frame = w.frames
+    heads = min(args.ref_heads, w.num_heads)
+    # warm-up reps are discarded, then K reps timed
+    oracle_block_sample(w.replace(frames=frame + 4), frame, heads, max(args.warmup, 1), budget_s=60.0)
+    times, value = oracle_block_sample(w.replace(frames=frame + args.steps + 4), frame, heads, args.steps,
+                                       budget_s=240.0)
+    ms = 1000.0 / value
+    cores = blas_threads()
+    sample = (f"per step: one frame of bookkeeping + gather + fp64 attention of block 0 over {heads} of "
+              f"{w.num_heads} heads at frame {frame} ({visible_tokens(w, frame)} visible keys); "
+              f"frame-steps/s extrapolated x{w.num_heads // heads} heads x{w.num_blocks} blocks; "
+              f"{len(times)} steps timed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, frame),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w: wl.Workload, frame: int) -> dict:
+    return {"workload": w.name, "blocks": w.num_blocks, "streams": w.num_streams, "heads": w.num_heads,
+            "head_dim": w.head_dim, "page_size": w.page_size, "patches_per_frame": w.patches_per_frame,
+            "specials_per_frame": w.specials_per_frame, "scale_frames": w.scale_frames,
+            "sliding_window": w.sliding_window, "frames_streamed": frame,
+            "visible_tokens_per_stream": visible_tokens(w, frame)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args, w: wl.Workload):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist_init("nccl")
+    import streaming_paged_kv_two_gb300 as spk
+    from gpu_harness import spk_config_for, to_device
+
+    K, W = args.steps, args.warmup
+    total_frames = w.frames
+    extra = W + K + 2                       # the e2e pass streams past the steady-state frame
+    wk = w.replace(frames=total_frames + extra)
+    cfg, keep = spk_config_for(wk)
+    pool_bytes, ws_bytes = spk.required_bytes(cfg)
+    dev = torch.device("cuda", local)
+    pools = [torch.empty(pool_bytes, dtype=torch.uint8, device=dev) for _ in range(w.num_blocks)]
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    cache = spk.Cache(cfg, pools, keep)
+    stream = torch.cuda.current_stream()
+    B, L, T = w.num_streams, w.num_blocks, w.tokens_per_frame
+
+    # device-resident inputs: NV frame variants per (stream, block), drawn by the workload generator
+    NV = 2
+    qs = [[[to_device(wl.frame_q(w, s, b, vi), w.dtype) for b in range(L)] for s in range(B)] for vi in range(NV)]
+    kvs = [[[tuple(to_device(x, w.dtype) for x in wl.frame_kv(w, s, b, vi)) for b in range(L)] for s in range(B)]
+           for vi in range(NV)]
+    qcat = [[torch.cat([qs[vi][s][b] for s in range(B)]) for b in range(L)] for vi in range(NV)]
+    outs = [torch.empty_like(qcat[0][b]) for b in range(L)]
+
+    def append_all(f, b):
+        vi = f % NV
+        for s in range(B):
+            k, v = kvs[vi][s][b]
+            cache.append_frame(s, b, k, v, stream)
+
+    # fast-forward: frames whose attention is not timed only need their K/V appended
+    t_ff = time.perf_counter()
+    pre = max(0, total_frames - K - W)
+    for f in range(pre):
+        for s in range(B):
+            k, v = kvs[f % NV][s][0]
+            cache.append_frame(s, 0, k, v, stream)
+            cache.evict_frames(s)
+        for b in range(1, L):
+            append_all(f, b)
+    torch.cuda.synchronize()
+    t_ff = time.perf_counter() - t_ff
+
+    ev_pairs = []
+
+    def frame_step(f, timed_launches=False, q_override=None, out_override=None):
+        vi = f % NV
+        for s in range(B):
+            k, v = kvs[vi][s][0]
+            cache.append_frame(s, 0, k, v, stream)
+        for s in range(B):
+            cache.evict_frames(s)
+        cache.plan(ws, stream)
+        for b in range(L):
+            if b:
+                append_all(f, b)
+            q = qcat[vi][b] if q_override is None else q_override[b]
+            o = outs[b] if out_override is None else out_override[b]
+            if timed_launches:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                cache.run_attention(b, q, o, ws, stream)
+                e1.record(stream)
+                ev_pairs.append((e0, e1))
+            else:
+                cache.run_attention(b, q, o, ws, stream)
+
+    f = pre
+    for _ in range(W):
+        frame_step(f)
+        f += 1
+    info = cache.get_plan_info()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    f_first = f
+    t0.record(stream)
+    for _ in range(K):
+        frame_step(f, timed_launches=True)
+        f += 1
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed = t0.elapsed_time(t1) / 1000.0
+    barrier()
+    max_elapsed = reduce_max(elapsed, device=dev)
+    status = spk.read_device_status(ws, stream)
+    launch_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+
+    # ------------------------------------------------ e2e: host buffers, copies in the timed region
+    hq = [[qcat[vi][b].cpu().pin_memory() for b in range(L)] for vi in range(NV)]
+    hkv = [[[tuple(x.cpu().pin_memory() for x in kvs[vi][s][b]) for b in range(L)] for s in range(B)]
+           for vi in range(NV)]
+    dq = [torch.empty_like(qcat[0][b]) for b in range(L)]
+    dkv = [[tuple(torch.empty_like(x) for x in kvs[0][s][b]) for b in range(L)] for s in range(B)]
+    hout = [torch.empty(outs[b].shape, dtype=outs[b].dtype).pin_memory() for b in range(L)]
+    h2d = sum(x.numel() * x.element_size() for b in range(L) for x in (hq[0][b],)) + \
+        sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b])
+    d2h = sum(x.numel() * x.element_size() for x in hout)
+
+    def e2e_step(f):
+        vi = f % NV
+        for b in range(L):
+            dq[b].copy_(hq[vi][b], non_blocking=True)
+            for s in range(B):
+                dkv[s][b][0].copy_(hkv[vi][s][b][0], non_blocking=True)
+                dkv[s][b][1].copy_(hkv[vi][s][b][1], non_blocking=True)
+        for s in range(B):
+            cache.append_frame(s, 0, dkv[s][0][0], dkv[s][0][1], stream)
+        for s in range(B):
+            cache.evict_frames(s)
+        cache.plan(ws, stream)
+        for b in range(L):
+            if b:
+                for s in range(B):
+                    cache.append_frame(s, b, dkv[s][b][0], dkv[s][b][1], stream)
+            cache.run_attention(b, dq[b], outs[b], ws, stream)
+            hout[b].copy_(outs[b], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step(f)
+        f += 1
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step(f)
+        f += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1000.0, device=dev)
+
+    # ------------------------------------------------ report
+    hbm, tflops, tflops_sus, peak_kind = load_peaks()
+    frames_timed = list(range(f_first + 1, f_first + K + 1))
+    flops = statistics.mean(block_work(w, x)[0] for x in frames_timed)
+    byts = statistics.mean(block_work(w, x)[1] for x in frames_timed)
+    avg_launch = statistics.mean(launch_ms) / 1000.0
+    t_roof_block = max(flops / (tflops * 1e12), byts / (hbm * 1e9))
+    bound = "hbm" if byts / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = byts / avg_launch / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = flops / avg_launch / 1e12, tflops, "TFLOP/s"
+    value = aggregate_throughput(K, world, max_elapsed)
+    step_ms = max_elapsed / K * 1000.0
+    launches_per_step = B * L + L + (L if info["merge_needed"] else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_config(w, f_first + K), "timed_frames": [f_first + 1, f_first + K],
+                   "l2": "no flush: visible K/V per block exceeds L2",
+                   "parallelism": f"replicas x{world} (independent streams, no data-path collective)"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "attention (tcgen05 paged attention + LSE merge), per block launch",
+                     "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+                     "avg_launch_us": avg_launch * 1e6, "algorithmic_bytes_per_launch": byts,
+                     "algorithmic_flops_per_launch": flops,
+                     "tensor_tflops": flops / avg_launch / 1e12, "hbm_gbs": byts / avg_launch / 1e9},
+        "attention_roofline_frac": t_roof_block * L / (max_elapsed / K),
+        "roofline_frame_steps_per_s": 1.0 / (t_roof_block * L),
+        "e2e": {"value": aggregate_throughput(K, world, e2e_elapsed), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "frames": [f - K + 1, f]},
+        "gpu_launches": launches_per_step * K,
+        "plan": info,
+        "clocks": clk,
+        "device_status": status,
+        "fast_forward_s": t_ff,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, cpu_value = oracle_block_sample(w, f_first + K, heads=2, reps=50, budget_s=20.0)
+        line["cpu_baseline"] = {
+            "value": cpu_value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"{len(times)} reps of one frame of bookkeeping + gather + fp64 attention of block 0 over 2 "
+                       f"of {w.num_heads} heads at frame {f_first + K}; extrapolated to all heads and "
+                       f"{w.num_blocks} blocks")}
+    if rank == 0:
+        print(json.dumps(line))
+    cache.close()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
+    ap.add_argument("--ref-heads", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "spk":
+        args.warmup = 3
+    w = wl.CONFIGS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

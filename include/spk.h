@@ -1,0 +1,211 @@
+/*
+ * spk.h — C ABI of libspk: streaming two-stream paged-KV attention on GB300.
+ *
+ * What it computes.  Each new frame of a video stream brings T = P + S tokens
+ * (P patch tokens, S special tokens).  Every transformer block keeps its K/V in
+ * a pool of pages [num_pages, 2 (K/V), page_size, H, D] (NHD).  Patch pages are
+ * recyclable: the first scale_frames frames are kept for good and the next
+ * sliding_window frames form a live window whose oldest page is recycled.
+ * Special pages are append-only: the S special tokens of every frame pack
+ * contiguously across them and are never evicted.  Once per frame the visible
+ * page table (scale -> live window -> specials, with last_page_len) is planned;
+ * every block then runs exact, non-causal softmax(Q K^T / sqrt(D)) V of the
+ * frame's T queries over all visible keys, including the frame's own.
+ *
+ * Sources (page title, section):
+ *   "How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction":
+ *     "Patch Stream and Special Stream", "Physical Memory Layout",
+ *     "Page Table Planning and Reuse", "Attention Kernel Execution",
+ *     "Appending Frames and Eviction", "Running Attention in Streaming Mode".
+ *   "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback in
+ *     Streaming Inference": "Two-Stream Design", "Plan-Run Execution Workflow",
+ *     "Inspecting Cache Statistics".
+ *   "How FlashInfer KV Cache Attention Accelerates Streaming 3D Reconstruction
+ *     Over SDPA": "FlashInferKVCacheManager Responsibilities",
+ *     "FlashInferAttention Forward Pass", "Efficient Attention Masking and Padding".
+ *   "How Paged KV Cache Attention Achieves Stable Inference in Ling-Bot-Map":
+ *     "Frame Appending Without Dispatch Overhead", "Sliding-Window Eviction
+ *     Strategy", "Resetting for New Sequences".
+ *
+ * Conventions.
+ *   - Every call returns an int status (SPK_OK or an SPK_ERR_* code); no C++
+ *     exception crosses the ABI.  spk_last_error() gives a message for the last
+ *     failing call on the calling thread.
+ *   - Device memory (pools, workspace, q/k/v/out) is owned by the caller.  The
+ *     library owns its host bookkeeping and the TMA descriptors it builds.
+ *   - GPU work is ordered on the cudaStream_t passed as `cuda_stream` (a
+ *     cudaStream_t value cast to void*; NULL is the legacy default stream).
+ *   - Several streams (independent videos) may share one cache; each has its
+ *     own bookkeeping and they are planned and attended in one batched launch.
+ *   - Page ids: stream s owns patch ids [s*MPP, (s+1)*MPP) and special ids
+ *     [B*MPP + s*MSP, B*MPP + (s+1)*MSP), with MPP = max_patch_pages,
+ *     MSP = max_special_pages and B = num_streams.  Pools have B*(MPP+MSP) pages.
+ *   - A cache created with pools == NULL is a bookkeeping-only ("dry") cache:
+ *     append/evict/plan run on the host with no device memory and no CUDA call;
+ *     calls that would touch device memory return SPK_ERR_INVALID_ARG.
+ */
+#ifndef SPK_H
+#define SPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum spk_status {
+  SPK_OK = 0,
+  SPK_ERR_INVALID_ARG = 1,          /* bad pointer, size, id or configuration */
+  SPK_ERR_OUT_OF_PATCH_PAGES = 2,   /* no free patch page for a new frame */
+  SPK_ERR_OUT_OF_SPECIAL_PAGES = 3, /* special pool exhausted ("appends tokens until the pool is exhausted") */
+  SPK_ERR_BAD_STATE = 4,            /* wrong call order: block order, stale or missing plan */
+  SPK_ERR_CUDA = 5,                 /* a CUDA runtime/driver call failed */
+  SPK_ERR_DEVICE_TIMEOUT = 6        /* a device-side wait ran past its limit; see spk_read_device_status */
+};
+
+enum spk_dtype {
+  SPK_BF16 = 0, /* hot path: bf16 storage, tcgen05 tensor cores, fp32 softmax/accumulate, bf16 out */
+  SPK_F32 = 1   /* accuracy path: fp32 storage and fp32 CUDA-core arithmetic, fp32 out */
+};
+
+typedef struct {
+  int32_t num_blocks;          /* L: one pool per transformer block */
+  int32_t num_streams;         /* B: independent streams batched in one launch */
+  int32_t num_heads;           /* H (query heads = KV heads) */
+  int32_t head_dim;            /* D: 64 or 128 */
+  int32_t page_size;           /* ps: tokens per page, >= patches_per_frame, <= 32768 */
+  int32_t patches_per_frame;   /* P >= 1: rows 0..P-1 of a frame's k/v/q */
+  int32_t specials_per_frame;  /* S >= 1: rows P..P+S-1 */
+  int32_t scale_frames;        /* sc >= 0: first frames kept for good */
+  int32_t sliding_window;      /* w >= 0: live window, counting the current frame */
+  int32_t max_patch_pages;     /* MPP per stream, >= 1 (the pages' sizing: sc + w + 16) */
+  int32_t max_special_pages;   /* MSP per stream, >= 1 (ceil(max_total_frames * S / ps)) */
+  int32_t dtype;               /* enum spk_dtype */
+  int32_t splits_per_stream;   /* 0 = planner's choice; k > 0 forces k KV splits per stream (clamped to [1, chunks]) */
+  int32_t reserved;            /* must be 0 */
+  const int32_t* patch_page_order;   /* optional host array [B*MPP]: initial free-list order, global ids;
+                                        entries [s*MPP, (s+1)*MPP) must permute stream s's patch ids. NULL = ascending */
+  const int32_t* special_page_order; /* optional host array [B*MSP], same rule for special ids. NULL = ascending */
+} spk_config;
+
+typedef struct {
+  int64_t frame_count;     /* frames appended since create/reset */
+  int64_t scale_pages;     /* patch pages held as scale frames */
+  int64_t live_pages;      /* patch pages in the live window */
+  int64_t free_pages;      /* free patch pages */
+  int64_t special_tokens;  /* special tokens appended (S per frame) */
+} spk_stats;
+
+typedef struct {
+  int32_t num_chunks;      /* KV chunks (<= 128 tokens inside one page) over all streams */
+  int32_t num_splits;      /* KV splits over all streams */
+  int32_t num_ctas;        /* CTAs of one attention launch */
+  int32_t merge_needed;    /* 1 when some stream has more than one split (merge kernel runs) */
+  int64_t visible_tokens;  /* sum over streams of visible keys */
+} spk_plan_info;
+
+typedef struct spk_cache spk_cache;
+
+/* Message for the last failing call on this thread ("" if none).  Owned by the library. */
+const char* spk_last_error(void);
+
+/* Sizes the caller must allocate: one pool per block (pool_bytes_per_block, 256-byte
+ * aligned start) and one workspace (workspace_bytes, 256-byte aligned start).
+ * Either output pointer may be NULL.  No CUDA call. */
+int spk_required_bytes(const spk_config* cfg, size_t* pool_bytes_per_block, size_t* workspace_bytes);
+
+/* Create a cache.  pools: host array of num_blocks device pointers, or NULL for a
+ * bookkeeping-only cache.  The library keeps the pointers (the caller keeps
+ * ownership) and zeroes every pool once, on the legacy default stream, before
+ * returning, so slots that are never written read as 0.  Builds one TMA
+ * descriptor per pool (bf16).  The current CUDA device must be the pools' device. */
+int spk_create_cache(const spk_config* cfg, void* const* pools, spk_cache** out);
+
+/* Free the host state.  The pools and workspace stay the caller's. NULL is accepted. */
+int spk_destroy_cache(spk_cache* cache);
+
+/* Clear the bookkeeping (free lists back to their initial order, counters to zero);
+ * the pools are kept as they are ("Resetting for New Sequences"). */
+int spk_reset(spk_cache* cache);
+
+/* Append one frame's K/V for one block.  k, v: device [T, H, D] contiguous NHD in
+ * the cache dtype, rows 0..P-1 patch tokens, rows P..T-1 special tokens.
+ * block 0 starts a new frame: it takes a free patch page (a scale page while
+ * fewer than scale_frames exist, else a live-window page) and reserves S special
+ * slots, taking new special pages as the tail fills; all-or-nothing, so on
+ * SPK_ERR_OUT_OF_* nothing changes.  It marks the plan stale.  Blocks 1..L-1 of
+ * the same frame write to the same targets; calling block b > 0 before block 0 of
+ * a frame, or twice in one frame, is SPK_ERR_BAD_STATE.  The copy runs on
+ * cuda_stream (one kernel).  On a bookkeeping-only cache k and v must be NULL. */
+int spk_append_frame(spk_cache* cache, int stream, int block, const void* k, const void* v,
+                     void* cuda_stream);
+
+/* Evict: move the oldest live-window pages to the free list until at most
+ * sliding_window remain.  Host only, no data moves.  Marks the plan stale. */
+int spk_evict_frames(spk_cache* cache, int stream);
+
+/* Plan the current frame for every stream: visible page table, indptr,
+ * last_page_len, patch-page counts, KV chunks and the split-KV work list.  Built on
+ * the host and uploaded with one async copy into `workspace` on cuda_stream; the
+ * same plan serves every block until the next append(block 0) or evict.  Every
+ * stream must hold at least one frame.  A bookkeeping-only cache takes
+ * workspace == NULL and builds the host tables only. */
+int spk_plan(spk_cache* cache, void* workspace, void* cuda_stream);
+
+/* Attention of the current frame for one block, all streams in one launch.
+ * q: device [B*T, H, D] (stream s owns rows s*T..s*T+T-1), out: device [B*T, H, D],
+ * both in the cache dtype.  workspace must be the one given to spk_plan.  Launches
+ * the attention kernel and, when a stream has several KV splits, the merge kernel.
+ * Requires a current plan and block's K/V appended for this frame on every stream. */
+int spk_run_attention(spk_cache* cache, int block, const void* q, void* out, void* workspace,
+                      void* cuda_stream);
+
+/* Copy one raw page [2, page_size, H, D] of block's pool to dst (host or device
+ * memory, page_bytes = 2*ps*H*D*elem).  Synchronizes cuda_stream before returning. */
+int spk_read_kv(spk_cache* cache, int block, int page_id, void* dst, void* cuda_stream);
+
+/* Host copy of the last plan.  indices has room for `capacity` entries; kv_indptr
+ * and qo_indptr [B+1]; last_page_len and num_patch_pages [B].  *nnz receives the
+ * number of indices even when capacity is too small (then SPK_ERR_INVALID_ARG).
+ * Array pointers other than nnz may be NULL to skip them. */
+int spk_get_plan_host(const spk_cache* cache, int32_t* indices, int32_t capacity, int32_t* kv_indptr,
+                      int32_t* last_page_len, int32_t* num_patch_pages, int32_t* qo_indptr,
+                      int32_t* nnz);
+
+/* Launch shape of the last plan. */
+int spk_get_plan_info(const spk_cache* cache, spk_plan_info* info);
+
+/* Targets of the stream's current frame: its patch page, and for each special row j
+ * the special page and slot.  special_pages / special_slots have room for S entries. */
+int spk_get_frame_targets(const spk_cache* cache, int stream, int32_t* patch_page,
+                          int32_t* special_pages, int32_t* special_slots);
+
+/* get_cache_stats() of one stream. */
+int spk_get_stats(const spk_cache* cache, int stream, spk_stats* stats);
+
+/* Synchronize cuda_stream, read and clear the device status word at the start of
+ * `workspace`.  *code receives 0 or the raw device code; returns
+ * SPK_ERR_DEVICE_TIMEOUT when a kernel recorded a wait that ran past its limit. */
+int spk_read_device_status(void* workspace, void* cuda_stream, int32_t* code);
+
+/* Self-test of the bounded device wait: one CTA waits on an mbarrier that nothing
+ * signals, gives up after limit_ns nanoseconds, records the timeout in the status
+ * word of `workspace` and returns normally.  Read it with spk_read_device_status. */
+int spk_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* cuda_stream);
+
+/* Diagnostics for the bf16 tensor-core kernel: run block's attention launch in
+ * score-dump mode.  Every CTA stops after the first chunk of its KV split and writes
+ * the raw Q K^T tile of that chunk (fp32, before scaling and masking) to
+ * dst[cta][row][key], cta = (split * H + head) * ceil(T/128) + query tile, rows and
+ * keys 0..127 (rows past T come from zero queries).  dst: device memory of
+ * num_ctas * 128 * 128 * 4 bytes (num_ctas from spk_get_plan_info).  out is not
+ * written; same preconditions as spk_run_attention. */
+int spk_debug_dump_scores(spk_cache* cache, int block, const void* q, float* dst, void* workspace,
+                          void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPK_H */

@@ -1,0 +1,114 @@
+// Internal declarations shared by the host library and the CUDA kernels of libspk.
+// Not part of the public ABI (include/spk.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace spk {
+
+// KV chunk: a run of at most kChunkTokens consecutive tokens inside one page.
+constexpr int kChunkTokens = 128;
+// Upper bound of KV splits per stream (the workspace holds partials for this many).
+constexpr int kMaxSplitsPerStream = 32;
+// Special rows per frame that one append carries in its kernel parameters.
+constexpr int kMaxSpecials = 64;
+// Query rows per tensor-core tile (tcgen05 M).
+constexpr int kTileRows = 128;
+// Device status word codes (first int32 of the workspace).
+constexpr int kStatusOk = 0;
+constexpr int kStatusWaitTimeout = 1;
+// Default limit of one device-side wait before it gives up (nanoseconds).
+constexpr long long kDefaultWaitLimitNs = 2000000000LL;
+
+// Chunk descriptor: page id, and start | len << 16 (start < 65536, 1 <= len <= 128).
+struct ChunkDesc {
+  int32_t page;
+  int32_t start_len;
+};
+
+// One KV split of one stream.
+struct WorkDesc {
+  int32_t stream;
+  int32_t chunk_begin;
+  int32_t chunk_end;
+  int32_t nsplit;  // splits of this stream; 1 = the attention kernel writes the output itself
+};
+
+// Per-stream merge table.
+struct StreamDesc {
+  int32_t split_base;  // index of the stream's first split
+  int32_t nsplit;
+  int32_t pad0, pad1;
+};
+
+// Workspace layout (byte offsets from its start, all 256-aligned).
+struct WorkspaceLayout {
+  size_t status = 0;     // int32 status, int32 detail
+  size_t streams = 0;    // StreamDesc[B]
+  size_t chunks = 0;     // ChunkDesc[max_chunks]
+  size_t works = 0;      // WorkDesc[max_splits]
+  size_t plan_end = 0;   // end of the part uploaded by plan
+  size_t part_o = 0;     // float[max_splits][H][T][D]
+  size_t part_lse = 0;   // float[max_splits][H][T]  (log2 units)
+  size_t total = 0;
+  int64_t max_chunks = 0;
+  int64_t max_splits = 0;
+};
+
+struct AppendParams {
+  char* pool;                 // block pool base
+  const char* k;              // [T, H, D]
+  const char* v;
+  int64_t row_bytes;          // H * D * elem
+  int64_t page_bytes;         // 2 * ps * row_bytes (K half then V half)
+  int64_t half_bytes;         // ps * row_bytes
+  int32_t T, P;
+  int32_t patch_page;
+  int32_t special_page[kMaxSpecials];
+  int32_t special_slot[kMaxSpecials];
+};
+
+struct AttnParams {
+  const void* pool;
+  const void* q;              // [B*T, H, D]
+  void* out;                  // [B*T, H, D]
+  const ChunkDesc* chunks;
+  const WorkDesc* works;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+  int64_t row_stride;         // elements between consecutive tokens in the pool (H*D)
+  int64_t page_stride;        // elements between pages (2*ps*H*D)
+  int64_t half_stride;        // elements between K and V halves of a page (ps*H*D)
+  int32_t T, H, D, ps;
+  int32_t num_splits;
+  int32_t ntiles;             // query tiles of kTileRows per stream
+  float scale_log2;           // log2(e) / sqrt(D)
+  long long wait_limit_ns;
+  float* dump_scores;         // diagnostics only: non-NULL makes the bf16 kernel write the raw
+                              // Q K^T tile of each CTA's first chunk ([ctas][128][128] fp32) and stop
+};
+
+struct MergeParams {
+  const float* part_o;
+  const float* part_lse;
+  const StreamDesc* streams;
+  void* out;
+  int32_t B, T, H, D;
+};
+
+// Kernel launchers (defined in the .cu files).  All return the launch error.
+cudaError_t launch_append(const AppendParams& p, int elem_bytes, cudaStream_t s);
+cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s);
+cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s);
+
+// Resident CTAs per SM the bf16 attention kernel is built for (planner input).
+int attention_bf16_ctas_per_sm(int head_dim);
+
+}  // namespace spk

@@ -1,0 +1,212 @@
+// Append (scatter) kernel, log-sum-exp merge kernel, fp32 CUDA-core attention
+// for the SPK_F32 accuracy path, and the bounded-wait self-test kernel.
+#include "ptx_sm100.cuh"
+#include "spk_internal.h"
+
+#include <cuda_bf16.h>
+
+namespace spk {
+
+// ------------------------------------------------------------------ append
+// A frame's K/V rows land in the pool by slice assignment: rows 0..P-1 into the
+// frame's patch page (slots 0..P-1), special row j into its reserved special
+// slot ("How Paged KV Cache Attention Achieves Stable Inference in Ling-Bot-Map",
+// "Frame Appending Without Dispatch Overhead"; "How FlashInfer's Paged KV Cache
+// Attention Outperforms SDPA Fallback in Streaming Inference", "Two-Stream
+// Design").  One thread moves 16 bytes; K and V in one launch.
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  const int32_t upr = int32_t(p.row_bytes >> 4);  // 16-byte units per token row
+  const int32_t per_kv = p.T * upr;
+  const int32_t total = 2 * per_kv;
+  for (int32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
+    const int32_t kv = u >= per_kv;
+    const int32_t rem = u - kv * per_kv;
+    const int32_t r = rem / upr;
+    const int32_t c = rem - r * upr;
+    const char* src = (kv ? p.v : p.k) + int64_t(r) * p.row_bytes + int64_t(c) * 16;
+    int32_t page, slot;
+    if (r < p.P) {
+      page = p.patch_page;
+      slot = r;
+    } else {
+      page = p.special_page[r - p.P];
+      slot = p.special_slot[r - p.P];
+    }
+    char* dst = p.pool + int64_t(page) * p.page_bytes + kv * p.half_bytes + int64_t(slot) * p.row_bytes +
+                int64_t(c) * 16;
+    *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+  }
+}
+
+cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_t s) {
+  const int64_t units = 2 * int64_t(p.T) * (p.row_bytes >> 4);
+  int64_t blocks = (units + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  append_kernel<<<int(blocks), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ merge
+// Exact recombination of softmax attention over disjoint key sets: with
+// M = max_j lse_j (log2 units) and w_j = 2^(lse_j - M),
+// out = sum_j w_j O_j / sum_j w_j.  One warp per (query row, head).
+template <int D, typename OutT>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  constexpr int E = D / 32;  // elements per lane
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rows = p.B * p.T;
+  if (warp >= rows * p.H) return;
+  const int row = warp / p.H;
+  const int h = warp - row * p.H;
+  const int s = row / p.T;
+  const int t = row - s * p.T;
+  const StreamDesc sd = p.streams[s];
+  if (sd.nsplit <= 1) return;  // written by the attention kernel
+  float m = -INFINITY;
+  for (int j = 0; j < sd.nsplit; ++j) {
+    const float l = __ldg(&p.part_lse[(int64_t(sd.split_base + j) * p.H + h) * p.T + t]);
+    m = fmaxf(m, l);
+  }
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int j = 0; j < sd.nsplit; ++j) {
+    const int64_t idx = (int64_t(sd.split_base + j) * p.H + h) * p.T + t;
+    const float w = exp2f(__ldg(&p.part_lse[idx]) - m);
+    wsum += w;
+    const float* o = p.part_o + idx * D + lane * E;
+    if constexpr (E == 2) {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(o));
+      acc[0] += w * v.x; acc[1] += w * v.y;
+    } else {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(o));
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    }
+  }
+  const float inv = 1.f / wsum;
+  OutT* out = static_cast<OutT*>(p.out) + (int64_t(row) * p.H + h) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if constexpr (sizeof(OutT) == 2) out[e] = __float2bfloat16_rn(acc[e] * inv);
+    else out[e] = acc[e] * inv;
+  }
+}
+
+cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s) {
+  const int64_t warps = int64_t(p.B) * p.T * p.H;
+  const int blocks = int((warps * 32 + 255) / 256);
+  if (dtype == 0) {
+    if (p.D == 64) merge_kernel<64, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+    else merge_kernel<128, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+  } else {
+    if (p.D == 64) merge_kernel<64, float><<<blocks, 256, 0, s>>>(p);
+    else merge_kernel<128, float><<<blocks, 256, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fp32 attention
+// Accuracy path (SPK_F32): exact attention over the split's chunks in fp32 on
+// CUDA cores, the paged counterpart of the manager's force_fp32 dense path ("How
+// LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "Attention
+// Kernel Execution").  One warp per (query row, head); lanes split D; online
+// softmax in log2 units.
+template <int D>
+__global__ void __launch_bounds__(256) attention_f32_kernel(const AttnParams p) {
+  constexpr int E = D / 32;
+  constexpr int kRowsPerCta = 8;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row_tiles = (p.T + kRowsPerCta - 1) / kRowsPerCta;
+  int x = blockIdx.x;
+  const int rt = x % row_tiles;
+  x /= row_tiles;
+  const int h = x % p.H;
+  const int split = x / p.H;
+  const int t = rt * kRowsPerCta + warp;
+  if (t >= p.T) return;
+  const WorkDesc w = p.works[split];
+  const float* pool = static_cast<const float*>(p.pool);
+  const int64_t qrow = int64_t(w.stream) * p.T + t;
+  const float* qp = static_cast<const float*>(p.q) + (qrow * p.H + h) * D + lane * E;
+  float q[E], acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    q[e] = qp[e] * p.scale_log2;
+    acc[e] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int c = w.chunk_begin; c < w.chunk_end; ++c) {
+    const ChunkDesc cd = p.chunks[c];
+    const int start = cd.start_len & 0xFFFF;
+    const int len = cd.start_len >> 16;
+    const float* kbase = pool + int64_t(cd.page) * p.page_stride + int64_t(start) * p.row_stride + h * D + lane * E;
+    const float* vbase = kbase + p.half_stride;
+    for (int j = 0; j < len; ++j) {
+      const float* kr = kbase + int64_t(j) * p.row_stride;
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) s = fmaf(q[e], __ldg(kr + e), s);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float m_new = fmaxf(m, s);
+      const float corr = exp2f(m - m_new);
+      const float pj = exp2f(s - m_new);
+      const float* vr = vbase + int64_t(j) * p.row_stride;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], corr, pj * __ldg(vr + e));
+      l = fmaf(l, corr, pj);
+      m = m_new;
+    }
+  }
+  const float inv = 1.f / l;
+  if (w.nsplit == 1) {
+    float* o = static_cast<float*>(p.out) + (qrow * p.H + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
+  } else {
+    const int64_t idx = (int64_t(split) * p.H + h) * p.T + t;
+    float* o = p.part_o + idx * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
+    if (lane == 0) p.part_lse[idx] = m + log2f(l);
+  }
+}
+
+cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s) {
+  const int row_tiles = (p.T + 7) / 8;
+  const int64_t blocks = int64_t(p.num_splits) * p.H * row_tiles;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (p.D == 64) attention_f32_kernel<64><<<int(blocks), 256, 0, s>>>(p);
+  else attention_f32_kernel<128><<<int(blocks), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ wait self-test
+// Waits on an mbarrier that nothing signals; the bounded wait gives up after
+// limit_ns and the kernel records the timeout in the status word.
+__global__ void selftest_wait_kernel(int32_t* status, long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0, limit_ns, &abort_flag)) {
+      atomicExch(status, kStatusWaitTimeout);
+      atomicExch(status + 1, 1);
+    }
+  }
+}
+
+cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace spk

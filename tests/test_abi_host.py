@@ -1,0 +1,261 @@
+"""Host-side tests of libspk (no GPU): exported symbols, configuration checks,
+bookkeeping-only caches against the oracle (bit-exact page tables, indptr,
+last_page_len, patch-page counts, frame targets and statistics), and error codes."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from oracle_cases import make_streams
+
+spk = pytest.importorskip("streaming_paged_kv_two_gb300")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def cfg_for(w: wl.Workload, **over):
+    po, so = wl.page_orders(w)
+    args = dict(num_blocks=w.num_blocks, num_streams=w.num_streams, num_heads=w.num_heads, head_dim=w.head_dim,
+                page_size=w.page_size, patches_per_frame=w.patches_per_frame,
+                specials_per_frame=w.specials_per_frame, scale_frames=w.scale_frames,
+                sliding_window=w.sliding_window, max_patch_pages=w.max_patch_pages,
+                max_special_pages=w.max_special_pages,
+                dtype=spk.SPK_BF16 if w.dtype == "bf16" else spk.SPK_F32,
+                patch_page_order=None if po is None else po.tolist(),
+                special_page_order=None if so is None else so.tolist())
+    args.update(over)
+    return spk.make_config(**args)
+
+
+def test_every_declared_symbol_is_exported():
+    header = open(os.path.join(ROOT, "include", "spk.h")).read()
+    declared = set(re.findall(r"^\s*(?:int|const char\*)\s+(spk_\w+)\s*\(", header, re.M))
+    assert len(declared) >= 15
+    for name in sorted(declared):
+        assert hasattr(spk.lib, name), name
+        assert ctypes.cast(getattr(spk.lib, name), ctypes.c_void_p).value
+
+
+def test_required_bytes_matches_layout():
+    w = wl.CONFIGS[3]
+    cfg, keep = cfg_for(w)
+    pool, ws = spk.required_bytes(cfg)
+    pages = w.num_streams * (w.max_patch_pages + w.max_special_pages)
+    assert pool == pages * 2 * w.page_size * w.num_heads * w.head_dim * 2
+    assert ws % 256 == 0 and ws > 0
+
+
+@pytest.mark.parametrize("over,needle", [
+    (dict(head_dim=32), "head_dim"),
+    (dict(page_size=100, patches_per_frame=101), "page_size"),
+    (dict(specials_per_frame=0), "specials"),
+    (dict(num_heads=0), "num_heads"),
+    (dict(dtype=7), "dtype"),
+    (dict(max_special_pages=0), "max pages"),
+])
+def test_invalid_configs_are_rejected(over, needle):
+    cfg, keep = cfg_for(wl.CONFIGS[2], **over)
+    with pytest.raises(spk.SpkError) as e:
+        spk.required_bytes(cfg)
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    assert needle in str(e.value)
+
+
+def test_bad_page_order_is_rejected():
+    w = wl.CONFIGS[5]
+    po, so = wl.page_orders(w)
+    po = po.copy()
+    po[3] = po[4]  # duplicate id
+    cfg, keep = cfg_for(w, patch_page_order=po.tolist())
+    with pytest.raises(spk.SpkError) as e:
+        spk.Cache(cfg, None, keep)
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    po2, _ = wl.page_orders(w)
+    po2 = po2.copy()
+    po2[0], po2[w.max_patch_pages] = po2[w.max_patch_pages], po2[0]  # ids swapped across streams
+    cfg, keep = cfg_for(w, patch_page_order=po2.tolist())
+    with pytest.raises(spk.SpkError):
+        spk.Cache(cfg, None, keep)
+
+
+def _compare_stream_run(w: wl.Workload, frames: int, every: int = 1):
+    cfg, keep = cfg_for(w)
+    cache = spk.Cache(cfg, None, keep)
+    streams = make_streams(w)
+    T = w.tokens_per_frame
+    for f in range(1, frames + 1):
+        for s, st in enumerate(streams):
+            pid, targets = st.append()
+            cache.append_frame(s, 0)
+            got_pid, got_targets = cache.get_frame_targets(s)
+            assert got_pid == pid and got_targets == targets, (f, s)
+        for s, st in enumerate(streams):
+            st.evict()
+            cache.evict_frames(s)
+        if f % every == 0 or f == frames:
+            cache.plan()
+            want = oracle.plan(streams, T)
+            got = cache.get_plan_host()
+            assert got == want, f
+            for s, st in enumerate(streams):
+                assert cache.get_stats(s) == st.stats()
+            info = cache.get_plan_info()
+            cpp = lambda n: -(-n // 128)
+            chunks = 0
+            for s, st in enumerate(streams):
+                chunks += st.num_patch_pages() * cpp(w.patches_per_frame)
+                ns = len(st.special_pages)
+                chunks += (ns - 1) * cpp(w.page_size) + cpp(st.last_page_len())
+            assert info["num_chunks"] == chunks
+            assert info["visible_tokens"] == sum(len(st.visible_sources()) for st in streams) if f % (every * 10) == 0 else True
+    cache.close()
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 5])
+def test_bookkeeping_matches_oracle_workloads(n):
+    w = wl.CONFIGS[n]
+    _compare_stream_run(w, w.frames, every=1 if w.frames <= 2000 else 7)
+
+
+def test_bookkeeping_matches_oracle_steady_state():
+    w = wl.CONFIGS[3]
+    _compare_stream_run(w, w.frames, every=13)
+
+
+@pytest.mark.parametrize("over", [
+    dict(scale_frames=0, sliding_window=0),
+    dict(scale_frames=0, sliding_window=1),
+    dict(page_size=128, patches_per_frame=128, specials_per_frame=64),
+    dict(page_size=256, patches_per_frame=199, specials_per_frame=57),
+    dict(num_streams=3, shuffle_pages=True),
+])
+def test_bookkeeping_matches_oracle_edge_cases(over):
+    base = wl.CONFIGS[2].replace(frames=150, num_blocks=2, **over)
+    _compare_stream_run(base, base.frames)
+
+
+def test_golden_stats_through_the_library():
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "cache_stats_after_42_frames.json")))
+    s = g["setup"]
+    cfg, keep = spk.make_config(num_blocks=1, num_streams=1, num_heads=16, head_dim=64, page_size=s["page_size"],
+                                patches_per_frame=s["patches_per_frame"], specials_per_frame=s["specials_per_frame"],
+                                scale_frames=s["scale_frames"], sliding_window=s["sliding_window"],
+                                max_patch_pages=s["max_patch_pages"], max_special_pages=s["max_special_pages"])
+    cache = spk.Cache(cfg, None, keep)
+    for _ in range(s["frames"]):
+        cache.append_frame(0, 0)
+        cache.evict_frames(0)
+    assert cache.get_stats(0) == g["expected"]
+
+
+def _dry(w=None, **over):
+    w = w or wl.CONFIGS[2].replace(num_blocks=3)
+    cfg, keep = cfg_for(w, **over)
+    return spk.Cache(cfg, None, keep)
+
+
+def test_out_of_special_pages_changes_nothing():
+    c = _dry(max_special_pages=1)   # 256 slots: 42 frames of 6 fit, the 43rd needs a second page
+    for _ in range(42):
+        c.append_frame(0, 0); c.evict_frames(0)
+    before = c.get_stats(0)
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 0)
+    assert e.value.code == spk.SPK_ERR_OUT_OF_SPECIAL_PAGES
+    assert c.get_stats(0) == before
+
+
+def test_out_of_patch_pages_changes_nothing():
+    c = _dry(max_patch_pages=5)
+    for _ in range(5):
+        c.append_frame(0, 0)      # no eviction
+    before = c.get_stats(0)
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 0)
+    assert e.value.code == spk.SPK_ERR_OUT_OF_PATCH_PAGES
+    assert c.get_stats(0) == before
+
+
+def test_block_order_errors():
+    c = _dry()
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 2)      # block 2 before any block 0
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    c.append_frame(0, 0)
+    c.append_frame(0, 2)
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 2)      # twice in one frame
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 3)      # out of range
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(1, 0)      # stream out of range
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+
+
+def test_plan_needs_a_frame_and_dry_cache_has_no_device_calls():
+    c = _dry()
+    with pytest.raises(spk.SpkError) as e:
+        c.plan()
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    with pytest.raises(spk.SpkError) as e:
+        c.get_plan_host()
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    c.append_frame(0, 0)
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 1, k=16, v=16)   # dry cache takes no device pointers
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    c.plan()
+    with pytest.raises(spk.SpkError) as e:
+        c.run_attention(0, 16, 16, 256)
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+
+
+def test_reset_restores_initial_order():
+    w = wl.CONFIGS[5].replace(frames=300)
+    cfg, keep = cfg_for(w)
+    c = spk.Cache(cfg, None, keep)
+    first = []
+    for rnd in range(2):
+        got = []
+        for f in range(40):
+            for s in range(w.num_streams):
+                c.append_frame(s, 0)
+                got.append(c.get_frame_targets(s))
+                c.evict_frames(s)
+        if rnd == 0:
+            first = got
+            c.reset()
+            assert c.get_stats(0) == dict(frame_count=0, scale_pages=0, live_pages=0,
+                                          free_pages=w.max_patch_pages, special_tokens=0)
+        else:
+            assert got == first
+
+
+def test_split_choice_is_valid():
+    w = wl.CONFIGS[3].replace(frames=2000)
+    cfg, keep = cfg_for(w)
+    c = spk.Cache(cfg, None, keep)
+    for f in range(300):
+        c.append_frame(0, 0); c.evict_frames(0)
+        c.plan()
+        info = c.get_plan_info()
+        assert 1 <= info["num_splits"] <= min(32, info["num_chunks"])
+        assert info["num_ctas"] == info["num_splits"] * 16 * 3
+    for k in (1, 5, 32, 1000):
+        cfg, keep = cfg_for(w, splits_per_stream=k)
+        c = spk.Cache(cfg, None, keep)
+        for f in range(100):
+            c.append_frame(0, 0); c.evict_frames(0)
+        c.plan()
+        info = c.get_plan_info()
+        assert info["num_splits"] == min(k, 32, info["num_chunks"])
+        assert info["merge_needed"] == (1 if info["num_splits"] > 1 else 0)

@@ -1,0 +1,242 @@
+"""GPU parity of the C-ABI path against the fp64 oracle (small and ragged cases).
+
+Every case streams frames through append -> evict -> plan -> per-block
+append/run_attention exactly as the library's users do, and compares each block's
+output with the oracle's dense float64 attention over the visible keys:
+bf16 within max-abs 2e-2 and mean-abs 2e-3, fp32 within max-abs 1e-4.
+Pool contents are compared bit for bit through read_kv.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import workloads as wl  # noqa: E402
+from oracle_cases import frame_fetcher, make_streams  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def _h():
+    import gpu_harness
+    return gpu_harness
+
+
+def small(**kw):
+    base = dict(name="small", num_blocks=2, num_streams=1, num_heads=2, head_dim=64, page_size=256,
+                patches_per_frame=256, specials_per_frame=6, scale_frames=2, sliding_window=3,
+                frames=9, dtype="bf16", value_scale=0.5)
+    base.update(kw)
+    return wl.Workload(**base)
+
+
+def stream_and_check(w: wl.Workload, splits: int = 0, check=lambda f: True, blocks=None):
+    """Stream w.frames frames; compare every checked frame's output with the oracle."""
+    gh = _h()
+    h = gh.Harness(w, splits)
+    streams = make_streams(w)
+    blocks = list(range(w.num_blocks)) if blocks is None else blocks
+    fetch_cache = {}
+    worst = (0.0, 0.0)
+    T = w.tokens_per_frame
+    for f in range(w.frames):
+        for s in range(w.num_streams):
+            k, v = wl.frame_kv(w, s, 0, f)
+            h.append(s, 0, k, v)
+            streams[s].append()
+        for s in range(w.num_streams):
+            h.cache.evict_frames(s)
+            streams[s].evict()
+        h.plan()
+        for b in blocks:
+            if b > 0:
+                for s in range(w.num_streams):
+                    k, v = wl.frame_kv(w, s, b, f)
+                    h.append(s, b, k, v)
+            q = np.concatenate([wl.frame_q(w, s, b, f) for s in range(w.num_streams)])
+            got = h.run(b, q)
+            if not check(f):
+                continue
+            fetchers = [frame_fetcher(w, s, b, fetch_cache.setdefault((s, b), {})) for s in range(w.num_streams)]
+            qs = [wl.to_f64(q[s * T:(s + 1) * T], w.dtype) for s in range(w.num_streams)]
+            want = np.concatenate([
+                oracle.attend(qs[s], *oracle.gather_visible(streams[s].visible_sources(), fetchers[s]))[0]
+                for s in range(w.num_streams)])
+            mx, mn = gh.check_close(got, want, w.dtype, f"{w.name} frame {f} block {b}")
+            worst = (max(worst[0], mx), max(worst[1], mn))
+    assert h.status() == 0
+    h.close()
+    return worst
+
+
+# ------------------------------------------------------------------ device status
+
+def test_selftest_wait_timeout_is_reported_and_context_survives():
+    import streaming_paged_kv_two_gb300 as spk
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    spk.selftest_wait_timeout(ws, 2_000_000, torch.cuda.current_stream())
+    with pytest.raises(spk.SpkError) as e:
+        spk.read_device_status(ws, torch.cuda.current_stream())
+    assert e.value.code == spk.SPK_ERR_DEVICE_TIMEOUT
+    assert spk.read_device_status(ws, torch.cuda.current_stream()) == 0   # cleared
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)
+    assert float(x.sum()) == 1024 * 1023 / 2                               # context still usable
+
+
+# ------------------------------------------------------------------ append / read_kv
+
+@pytest.mark.parametrize("w", [
+    small(frames=7),
+    small(frames=7, dtype="f32", head_dim=128),
+    small(frames=9, page_size=256, patches_per_frame=200, specials_per_frame=57, scale_frames=1, sliding_window=2),
+    small(frames=6, num_streams=2, shuffle_pages=True, head_dim=128),
+], ids=["bf16_d64", "f32_d128", "pad_and_straddle", "two_streams_shuffled"])
+def test_append_is_bit_exact(w):
+    gh = _h()
+    h = gh.Harness(w)
+    streams = make_streams(w)
+    for f in range(w.frames):
+        frame_data = {}
+        for s in range(w.num_streams):
+            for b in range(w.num_blocks):
+                k, v = wl.frame_kv(w, s, b, f)
+                frame_data[(s, b)] = (k, v)
+            k, v = frame_data[(s, 0)]
+            h.append(s, 0, k, v)
+            pid, targets = streams[s].append()
+            assert h.cache.get_frame_targets(s) == (pid, targets)
+        for s in range(w.num_streams):
+            for b in range(1, w.num_blocks):
+                h.append(s, b, *frame_data[(s, b)])
+            h.cache.evict_frames(s)
+            streams[s].evict()
+        torch.cuda.synchronize()
+        # every page written this frame holds exactly the frame's rows
+        for s, st in enumerate(streams):
+            pid, targets = h.cache.get_frame_targets(s)
+            for b in range(w.num_blocks):
+                k, v = frame_data[(s, b)]
+                page = h.read_page(b, pid)
+                P = w.patches_per_frame
+                assert np.array_equal(page[0, :P], k[:P]) and np.array_equal(page[1, :P], v[:P])
+                for j, (sp, slot) in enumerate(targets):
+                    spage = h.read_page(b, sp)
+                    assert np.array_equal(spage[0, slot], k[P + j]) and np.array_equal(spage[1, slot], v[P + j])
+    # and every visible slot still holds what the oracle says was written there
+    for s, st in enumerate(streams):
+        for b in range(w.num_blocks):
+            for page, slots in st.contents.items():
+                if page not in st.visible_pages():
+                    continue
+                got = h.read_page(b, page)
+                for slot, (frame, row) in slots.items():
+                    k, v = wl.frame_kv(w, s, b, frame)
+                    assert np.array_equal(got[0, slot], k[row]) and np.array_equal(got[1, slot], v[row])
+    h.close()
+
+
+# ------------------------------------------------------------------ raw scores
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tensor_core_scores_match(D):
+    """S = Q K^T of each CTA's first chunk, straight from TMEM, against numpy."""
+    gh = _h()
+    w = small(frames=1, head_dim=D, num_blocks=1)
+    h = gh.Harness(w, splits=3)          # chunks: patch 0..127, patch 128..255, specials 0..5
+    k, v = wl.frame_kv(w, 0, 0, 0)
+    h.append(0, 0, k, v)
+    h.cache.evict_frames(0)
+    h.plan()
+    info = h.cache.get_plan_info()
+    assert info["num_splits"] == 3 and info["num_chunks"] == 3
+    q = wl.frame_q(w, 0, 0, 0)
+    qd = gh.to_device(q, "bf16")
+    dst = torch.zeros((info["num_ctas"], 128, 128), dtype=torch.float32, device="cuda")
+    h.cache.debug_dump_scores(0, qd, dst, h.ws, h.stream)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy().astype(np.float64)
+    qf = wl.to_f64(q, "bf16")
+    kf = wl.to_f64(k, "bf16")
+    T, H = w.tokens_per_frame, w.num_heads
+    ntiles = -(-T // 128)
+    chunk_keys = [kf[0:128], kf[128:256], np.concatenate([kf[256:262], np.zeros((122, H, D))])]
+    for split in range(3):
+        for head in range(H):
+            for tile in range(ntiles):
+                cta = (split * H + head) * ntiles + tile
+                qt = np.zeros((128, D))
+                rows = qf[tile * 128:min(T, tile * 128 + 128), head]
+                qt[:len(rows)] = rows
+                want = qt @ chunk_keys[split][:, head].T
+                np.testing.assert_allclose(got[cta], want, atol=2e-3, rtol=1e-4,
+                                           err_msg=f"split {split} head {head} tile {tile}")
+    h.close()
+
+
+# ------------------------------------------------------------------ attention parity
+
+CASES = {
+    "tiny_stream_f32": (wl.CONFIGS[1], 0),
+    "tiny_stream_bf16": (wl.CONFIGS[1].replace(dtype="bf16", name="tiny_stream_bf16"), 0),
+    "t262_d64": (small(), 0),
+    "t262_d64_split1": (small(), 1),
+    "t262_d64_split5": (small(), 5),
+    "t262_d128_two_streams": (small(head_dim=128, num_streams=2, shuffle_pages=True, frames=7), 0),
+    "t129_pad": (small(patches_per_frame=123, page_size=128, frames=8), 3),
+    "t1005_ps1024": (small(patches_per_frame=999, page_size=1024, frames=5, value_scale=1.0, num_heads=2), 0),
+    "specials_straddle": (small(patches_per_frame=200, specials_per_frame=57, frames=8), 2),
+    "specials_only": (small(scale_frames=0, sliding_window=0, frames=6), 0),
+    "window1_no_scale": (small(scale_frames=0, sliding_window=1, frames=5), 0),
+    "f32_d128_streams": (small(dtype="f32", head_dim=128, num_streams=2, frames=5, value_scale=1.0), 3),
+    "per_head_scale_d128": (small(head_dim=128, per_head_scale=True, num_streams=2, frames=5, shuffle_pages=True), 0),
+    "t1_row": (small(patches_per_frame=1, specials_per_frame=1, page_size=16, frames=12), 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_stream_parity(name):
+    w, splits = CASES[name]
+    worst = stream_and_check(w, splits)
+    print(f"{name}: worst max-abs {worst[0]:.3e} mean-abs {worst[1]:.3e}")
+
+
+# ------------------------------------------------------------------ state errors on a real cache
+
+def test_run_attention_state_errors():
+    import streaming_paged_kv_two_gb300 as spk
+    gh = _h()
+    w = small(frames=3, num_blocks=3)
+    h = gh.Harness(w)
+    q = gh.to_device(wl.frame_q(w, 0, 0, 0), "bf16")
+    out = torch.empty_like(q)
+    k, v = wl.frame_kv(w, 0, 0, 0)
+    h.append(0, 0, k, v)
+    h.cache.evict_frames(0)
+    with pytest.raises(spk.SpkError) as e:
+        h.cache.run_attention(0, q, out, h.ws, h.stream)        # no plan yet
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    h.plan()
+    with pytest.raises(spk.SpkError) as e:
+        h.cache.run_attention(1, q, out, h.ws, h.stream)        # block 1 not appended
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    other = torch.zeros_like(h.ws)
+    with pytest.raises(spk.SpkError) as e:
+        h.cache.run_attention(0, q, out, other, h.stream)       # not the planned workspace
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    h.cache.run_attention(0, q, out, h.ws, h.stream)
+    h.append(0, 0, k, v)                                        # new frame: plan is stale
+    with pytest.raises(spk.SpkError) as e:
+        h.cache.run_attention(0, q, out, h.ws, h.stream)
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    h.close()
