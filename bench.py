@@ -350,11 +350,13 @@ def run_gpu(args, w: wl.Workload):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     f_first = f
+    torch.cuda.nvtx.range_push("timed")
     t0.record(stream)
     for _ in range(K):
         frame_step(f, timed_launches=True)
         f += 1
     t1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     clk = clocks.stop()
     elapsed = t0.elapsed_time(t1) / 1000.0
@@ -471,10 +473,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="profiling only: override the block count (smaller device footprint)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "spk":
         args.warmup = 3
     w = wl.CONFIGS[args.workload]
+    if args.blocks:
+        w = w.replace(num_blocks=args.blocks, name=f"{w.name}_blocks{args.blocks}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

@@ -196,11 +196,13 @@ int spk_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* cuda_stre
 
 /* Diagnostics for the bf16 tensor-core kernel: run block's attention launch in
  * score-dump mode.  Every CTA stops after the first chunk of its KV split and writes
- * the raw Q K^T tile of that chunk (fp32, before scaling and masking) to
- * dst[cta][row][key], cta = (split * H + head) * ceil(T/128) + query tile, rows and
- * keys 0..127 (rows past T come from zero queries).  dst: device memory of
- * num_ctas * 128 * 128 * 4 bytes (num_ctas from spk_get_plan_info).  out is not
- * written; same preconditions as spk_run_attention. */
+ * the raw Q K^T tiles of that chunk (fp32, before scaling and masking) for its up to
+ * two 128-row main query tiles to dst[cta][tile][row][key] (rows and keys 0..127;
+ * rows past T come from zero queries; a tile slot the CTA does not own is left as
+ * is).  cta = (split * H + head) * groups + group, where a group covers query rows
+ * [256*group, 256*group + 256).  dst: device memory of num_ctas * 2 * 128 * 128 * 4
+ * bytes (num_ctas from spk_get_plan_info).  out is not written; same preconditions
+ * as spk_run_attention. */
 int spk_debug_dump_scores(spk_cache* cache, int block, const void* q, float* dst, void* workspace,
                           void* cuda_stream);
 

@@ -7,23 +7,33 @@
 // Execution"; "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback
 // in Streaming Inference", "Memory Bandwidth Efficiency": only visible pages are
 // read).  Visible keys arrive as the planner's chunks (<= 128 tokens inside one
-// page), so patch-page padding and the tail special page's unused slots are
-// never part of the softmax ("How FlashInfer KV Cache Attention Accelerates
-// Streaming 3D Reconstruction Over SDPA", "Efficient Attention Masking and
-// Padding").
+// page), so patch-page padding and the tail special page's unused slots never
+// enter the softmax ("How FlashInfer KV Cache Attention Accelerates Streaming 3D
+// Reconstruction Over SDPA", "Efficient Attention Masking and Padding").
 //
-// One CTA = (KV split, head, 128-row query tile).  Warp roles:
-//   warp 0    TMA producer: K and V chunk tiles gathered by page id from a 4-D
-//             tensor map over the pool (d, head, token, page*2+kv), 128-byte swizzle,
-//             into a 2-stage shared-memory ring.
-//   warp 1    MMA issuer (one thread): S = Q K^T into TMEM (M=128, N=128, K=D),
-//             then O += P V with P read from TMEM (M=128, N=D, K=128).
-//   warps 2-5 softmax: one thread per query row (TMEM lane); fp32 online
-//             softmax in log2 units with masking of the chunk's ragged tail; P
-//             written back as bf16 over S; O rescaled in TMEM only when the
-//             running maximum grows by more than 2^8; epilogue normalises O and
-//             writes bf16 output (one split) or an fp32 partial and its
-//             log-sum-exp (several splits, combined by the merge kernel).
+// One CTA (one per SM) = (KV split, head, query-row group).  A group is up to two
+// 128-row "main" tiles, plus, on the last group when head_dim is 64, a "tail" of at
+// most 32 trailing rows (262 = 2 x 128 + 6).  Warp roles (14 warps):
+//   warps 0-3   tail softmax.  The tail's Q rows are replicated in the four TMEM
+//               lane quarters; warp q owns keys [16q, 16q+16) of every 64-key half
+//               chunk, so the tail's exponentials are spread evenly over the four
+//               SM sub-partitions.  Each warp keeps its own (max, sum, O) and the
+//               four partial states are merged at the end.
+//   warps 4-7   softmax of main tile 0, warps 8-11 softmax of main tile 1: one
+//               thread per query row (= TMEM lane).  fp32 online softmax in log2
+//               units, masking of the chunk's ragged tail, P written back as bf16
+//               over S, row sums taken from the rounded P that the MMA consumes,
+//               O rescaled in TMEM only when the running maximum grows by > 2^8.
+//   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
+//               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
+//               swizzle, into a ring of shared-memory stages.
+//   warp 13     MMA issuer (one thread): S_t = Q_t K^T (M=128, N=128, K=D) and
+//               O_t += P_t V (M=128, N=D, K=128) per main tile, ping-ponged so one
+//               tile's MMAs run while the other tile's softmax runs; the tail
+//               works on 64-key halves (N=64, K=64).
+// TMEM (512 columns): S0 | S1 | O0 | O1 [| S2 (64) | O2 (64) when D = 64].
+// The epilogue writes bf16 output (one split) or an fp32 partial with its log2
+// log-sum-exp (several splits, combined by the merge kernel).
 // Every wait is bounded: on timeout the kernel records a status word, drains its
 // own copies and MMAs, frees TMEM and returns.
 #include "ptx_sm100.cuh"
@@ -34,22 +44,34 @@
 namespace spk {
 namespace {
 
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;  // S/P at [0,128), O at [128, 128+D)
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kTailMaxRows = 32;
+constexpr int kThreads = 448;
+constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr int kSoftmaxThreads = 384;  // warps 0-11 (all arrive on q_full)
 
 template <int D>
-struct Smem {
-  static constexpr int kTileBytes = 128 * D * 2;  // Q, K or V tile
-  static constexpr int kQ = 0;
-  static constexpr int kK0 = kTileBytes;
-  static constexpr int kBars = kTileBytes + kStages * 2 * kTileBytes;
-  static constexpr int kNumBars = 2 * kStages + 4;
-  static constexpr int kMisc = kBars + kNumBars * 8;
+struct Cfg {
+  static constexpr int kTile = 128 * D * 2;  // one Q, K or V tile in shared memory
+  static constexpr bool kTail = (D == 64);
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kQ0 = 0;
+  static constexpr int kQ1 = kTile;
+  static constexpr int kQ2 = 2 * kTile;  // tail Q (D == 64)
+  static constexpr int kKV = (kTail ? 3 : 2) * kTile;
+  static constexpr int kStageBytes = 2 * kTile;
+  static constexpr int kBars = kKV + kStages * kStageBytes;
+  static constexpr int kNumBars = 2 * kStages + 8;  // full, empty, q_full, s_full[3], p_ready[3], o_done
+  static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kLaunchBytes = kBytes + 1024;  // slack for 1024-byte alignment
+  static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
+  static constexpr uint32_t kS2 = 256 + 2 * D, kO2 = 256 + 2 * D + 64;  // D == 64 only
+  static_assert(!kTail || kO2 + 64 <= 512, "TMEM budget");
+  static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
 };
 
 __device__ __forceinline__ void signal_abort(int32_t* status, volatile int* abort_flag) {
@@ -62,81 +84,183 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// sum of the two bf16 values held in a packed pair, in fp32
+__device__ __forceinline__ float packed_sum(uint32_t pk) {
+  return __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+}
+
+// Store one row of a 128-row Q tile in K-major 128-byte-swizzled layout: 16-byte
+// chunk c of row r goes to chunk c ^ (r & 7) of its 128-byte row.
 template <int D>
-__global__ void __launch_bounds__(kThreads, (D == 64) ? 2 : 1)
+__device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src, bool valid) {
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (valid) v = __ldg(src + c);
+    const int cb = c >> 3, cc = c & 7;
+    const uint32_t dst = sq + cb * kColBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
+
+// p = 2^(s*sl2 - m) for N fp32 scores in registers, packed to bf16 pairs and stored to
+// TMEM at column `dst`; returns the fp32 sum of the rounded values.
+template <int N>
+__device__ __forceinline__ float exp_pack_store(const uint32_t* s, float sl2, float neg_m, uint32_t dst) {
+  static_assert(N % 32 == 0, "");
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < N / 32; ++j) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float p0 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e]), sl2, neg_m));
+      const float p1 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m));
+      pk[e] = pack_bf16(p0, p1);
+      if (e & 1) sum1 += packed_sum(pk[e]);
+      else sum0 += packed_sum(pk[e]);
+    }
+    ptx::tmem_st16(dst + 16 * j, pk);
+  }
+  return sum0 + sum1;
+}
+
+__device__ __forceinline__ float max_masked32(const uint32_t* s, int first_key, int len, float mx) {
+  if (first_key + 32 <= len) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[e]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (first_key + e < len) mx = fmaxf(mx, __uint_as_float(s[e]));
+  }
+  return mx;
+}
+
+__device__ __forceinline__ void mask32(uint32_t* s, int first_key, int len) {
+  if (first_key + 32 > len) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (first_key + e >= len) s[e] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Scale `ncols` TMEM columns of this warp's lanes by corr (per lane).
+__device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float corr) {
+  for (int j = 0; j < ncols; j += 32) {
+    uint32_t o[32];
+    ptx::tmem_ld32(taddr + j, o);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+    ptx::tmem_st32(taddr + j, o);
+  }
+}
+
+// Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
+// `scale`: bf16 output when the stream has one split, else the fp32 partial.
+template <int D>
+__device__ __forceinline__ void store_output_cols(const AttnParams& p, const WorkDesc& work, int split, int head,
+                                                  int row, const uint32_t (&v)[32], int col0, float scale) {
+  if (work.nsplit == 1) {
+    const int64_t qrow = int64_t(work.stream) * p.T + row;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (qrow * p.H + head) * D + col0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      dst[k] = make_uint4(pack_bf16(__uint_as_float(v[8 * k]) * scale, __uint_as_float(v[8 * k + 1]) * scale),
+                          pack_bf16(__uint_as_float(v[8 * k + 2]) * scale, __uint_as_float(v[8 * k + 3]) * scale),
+                          pack_bf16(__uint_as_float(v[8 * k + 4]) * scale, __uint_as_float(v[8 * k + 5]) * scale),
+                          pack_bf16(__uint_as_float(v[8 * k + 6]) * scale, __uint_as_float(v[8 * k + 7]) * scale));
+  } else {
+    const int64_t idx = (int64_t(split) * p.H + head) * p.T + row;
+    float4* dst = reinterpret_cast<float4*>(p.part_o + idx * D + col0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      dst[k] = make_float4(__uint_as_float(v[4 * k]) * scale, __uint_as_float(v[4 * k + 1]) * scale,
+                           __uint_as_float(v[4 * k + 2]) * scale, __uint_as_float(v[4 * k + 3]) * scale);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap kv_map) {
-  using L = Smem<D>;
+  using C = Cfg<D>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  const uint32_t sQ = sbase + L::kQ;
-  auto sK = [&](int st) { return sbase + L::kK0 + st * 2 * L::kTileBytes; };
-  auto sV = [&](int st) { return sbase + L::kK0 + st * 2 * L::kTileBytes + L::kTileBytes; };
-  const uint32_t bars = sbase + L::kBars;
+  const uint32_t sQ0 = sbase + C::kQ0, sQ1 = sbase + C::kQ1, sQ2 = sbase + C::kQ2;
+  auto sK = [&](int st) { return sbase + C::kKV + st * C::kStageBytes; };
+  auto sV = [&](int st) { return sbase + C::kKV + st * C::kStageBytes + C::kTile; };
+  const uint32_t bars = sbase + C::kBars;
   auto full_bar = [&](int st) { return bars + 8 * st; };
-  auto empty_bar = [&](int st) { return bars + 8 * (kStages + st); };
-  const uint32_t q_full = bars + 8 * (2 * kStages);
-  const uint32_t s_full = q_full + 8;
-  const uint32_t p_ready = q_full + 16;
-  const uint32_t o_done = q_full + 24;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  auto empty_bar = [&](int st) { return bars + 8 * (S + st); };
+  const uint32_t q_full = bars + 8 * (2 * S);
+  auto s_full = [&](int t) { return q_full + 8 * (1 + t); };
+  auto p_ready = [&](int t) { return q_full + 8 * (4 + t); };
+  const uint32_t o_done = q_full + 8 * 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   int x = blockIdx.x;
-  const int tile = x % p.ntiles;
-  x /= p.ntiles;
+  const int group = x % p.ngroups;
+  x /= p.ngroups;
   const int head = x % p.H;
   const int split = x / p.H;
   const WorkDesc work = p.works[split];
   const int c0 = work.chunk_begin;
   const int n = work.chunk_end - work.chunk_begin;
-  const int row0 = tile * kTileRows;
+  const int row0 = group * 2 * kTileRows;
+  const int n_main = min(2, p.main_tiles - 2 * group);
+  const bool has_tail = C::kTail && group == p.ngroups - 1 && p.tail_rows > 0;
+  const int tail_row0 = p.main_tiles * kTileRows;
   const long long limit = p.wait_limit_ns;
   const bool dump = p.dump_scores != nullptr;
+  const float sl2 = p.scale_log2;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < S; ++i) {
       ptx::mbar_init(full_bar(i), 1);
       ptx::mbar_init(empty_bar(i), 1);
     }
-    ptx::mbar_init(q_full, 128);
-    ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(p_ready, 128);
+    ptx::mbar_init(q_full, kSoftmaxThreads);
+    for (int t = 0; t < 3; ++t) {
+      ptx::mbar_init(s_full(t), 1);
+      ptx::mbar_init(p_ready(t), 128);
+    }
     ptx::mbar_init(o_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + 128;
 
-  if (warp == 0) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       ptx::prefetch_tmap(&kv_map);
       int issued = 0;
-      const int nload = dump ? (n > 0 ? 1 : 0) : n;
+      const int nload = dump ? min(n, 1) : n;
       for (int i = 0; i < nload; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!ptx::mbar_wait_bounded(empty_bar(st), ph ^ 1, limit, abort_flag)) {
+        const int st = i % S;
+        if (!ptx::mbar_wait_bounded(empty_bar(st), ((i / S) & 1) ^ 1, limit, abort_flag)) {
           signal_abort(p.status, abort_flag);
           break;
         }
         const ChunkDesc cd = p.chunks[c0 + i];
         const int start = cd.start_len & 0xFFFF;
-        ptx::mbar_arrive_expect_tx(full_bar(st), 2 * L::kTileBytes);
+        ptx::mbar_arrive_expect_tx(full_bar(st), 2 * C::kTile);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
           ptx::tma_load_4d(sK(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page, full_bar(st));
@@ -145,39 +269,83 @@ __global__ void __launch_bounds__(kThreads, (D == 64) ? 2 : 1)
         }
         ++issued;
       }
-      // drain: every issued copy must land before the CTA may exit
-      for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        ptx::mbar_wait_bounded(full_bar(i % kStages), (i / kStages) & 1, limit, nullptr);
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i)  // drain: copies must land before exit
+        ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, nullptr);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idesc_qk_half = ptx::idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
-      bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
-      ptx::tc_fence_after();
-      const int nmma = dump ? (n > 0 ? 1 : 0) : n;
-      for (int i = 0; ok && i < nmma; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!(ok = ptx::mbar_wait_bounded(full_bar(st), ph, limit, abort_flag))) break;
-        ptx::tc_fence_after();
+      auto qk = [&](uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * kColBlockBytes + (k & 3) * 32;
-          const uint64_t a = ptx::smem_desc_sw128(sQ + off, 16, 1024);
-          const uint64_t b = ptx::smem_desc_sw128(sK(st) + off, 16, 1024);
-          ptx::mma_ss(tS, a, b, idesc_qk, k > 0 ? 1u : 0u);
+          ptx::mma_ss(d_tmem, ptx::smem_desc_sw128(sq + off, 16, 1024), ptx::smem_desc_sw128(sk + off, 16, 1024),
+                      idesc, k > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(s_full);
-        if (dump) break;
-        if (!(ok = ptx::mbar_wait_bounded(p_ready, i & 1, limit, abort_flag))) break;
+      };
+      auto pv = [&](uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, int ksteps, bool overwrite) {
+        for (int k = 0; k < ksteps; ++k)
+          ptx::mma_ts(o_tmem, p_tmem + 8 * k, ptx::smem_desc_sw128(sv + k * 2048, kColBlockBytes, 1024), idesc_pv,
+                      (overwrite && k == 0) ? 0u : 1u);
+      };
+      int full_seen = -1;
+      auto ensure_full = [&](int j) -> bool {
+        if (j <= full_seen) return true;
+        if (!ptx::mbar_wait_bounded(full_bar(j % S), (j / S) & 1, limit, abort_flag)) return false;
         ptx::tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t b = ptx::smem_desc_sw128(sV(st) + k * 2048, kColBlockBytes, 1024);
-          ptx::mma_ts(tO, tS + k * 8, b, idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+        full_seen = j;
+        return true;
+      };
+      const bool t0 = n_main >= 1, t1 = n_main >= 2;
+      bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
+      ptx::tc_fence_after();
+      if (ok && n > 0 && (ok = ensure_full(0))) {
+        if (t0) { qk(tmem + C::kS0, sQ0, sK(0), idesc_qk); ptx::mma_commit(s_full(0)); }
+        if (t1) { qk(tmem + C::kS1, sQ1, sK(0), idesc_qk); ptx::mma_commit(s_full(1)); }
+        if (has_tail) { qk(tmem + C::kS2, sQ2, sK(0), idesc_qk_half); ptx::mma_commit(s_full(2)); }
+      }
+      for (int j = 0; ok && !dump && j < n; ++j) {
+        const int st = j % S;
+        const bool more = j + 1 < n;
+        const int nst = (j + 1) % S;
+        if (t0) {
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(0), j & 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          pv(tmem + C::kO0, tmem + C::kS0, sV(st), 8, j == 0);
+          if (more) {
+            if (!(ok = ensure_full(j + 1))) break;
+            qk(tmem + C::kS0, sQ0, sK(nst), idesc_qk);
+            ptx::mma_commit(s_full(0));
+          }
+        }
+        if (t1) {
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(1), j & 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          pv(tmem + C::kO1, tmem + C::kS1, sV(st), 8, j == 0);
+          if (more) {
+            if (!(ok = ensure_full(j + 1))) break;
+            qk(tmem + C::kS1, sQ1, sK(nst), idesc_qk);
+            ptx::mma_commit(s_full(1));
+          }
+        }
+        if (has_tail) {
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 0, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          pv(tmem + C::kO2, tmem + C::kS2, sV(st), 4, j == 0);                 // keys 0..63
+          qk(tmem + C::kS2, sQ2, sK(st) + 64 * 128, idesc_qk_half);            // keys 64..127
+          ptx::mma_commit(s_full(2));
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          pv(tmem + C::kO2, tmem + C::kS2, sV(st) + 64 * 128, 4, false);
+          if (more) {
+            if (!(ok = ensure_full(j + 1))) break;
+            qk(tmem + C::kS2, sQ2, sK(nst), idesc_qk_half);
+            ptx::mma_commit(s_full(2));
+          }
         }
         ptx::mma_commit(empty_bar(st));
       }
@@ -186,163 +354,230 @@ __global__ void __launch_bounds__(kThreads, (D == 64) ? 2 : 1)
       ptx::mbar_wait_bounded(o_done, 0, limit, nullptr);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    const int q4 = warp & 3;                 // TMEM lane quarter of this warp
-    const int r = q4 * 32 + lane;            // row within the tile
-    const int row = row0 + r;
-    const bool row_ok = row < p.T;
-    const bool warp_active = row0 + q4 * 32 < p.T;
+  } else if (warp >= kWarpMain) {
+    // ------------------------------------------------------------ main-tile softmax
+    const int t = (warp - kWarpMain) >> 2;
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int row = row0 + t * kTileRows + r;
+    const bool tile_on = t < n_main;
+    const bool row_ok = tile_on && row < p.T;
+    const bool warp_on = tile_on && row0 + t * kTileRows + q4 * 32 < p.T;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const uint32_t tS = tmem + (t ? C::kS1 : C::kS0) + lane_off;
+    const uint32_t tO = tmem + (t ? C::kO1 : C::kO0) + lane_off;
     const int64_t qrow = int64_t(work.stream) * p.T + row;
+    if (tile_on)
+      store_q_row<D>(t ? sQ1 : sQ0, r,
+                     reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D),
+                     row_ok);
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(q_full);
 
-    // Q tile: 128 rows x D bf16, K-major, 128-byte swizzle (16-byte chunk c of row r
-    // stored at chunk c ^ (r & 7) of its 128-byte row).
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                        (qrow * p.H + head) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row_ok) v = __ldg(src + c);
-        const int cb = c >> 3, cc = c & 7;
-        const uint32_t dst = sQ + cb * kColBlockBytes + (r >> 3) * 1024 + (r & 7) * 128 + ((cc ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
-                     "r"(v.w)
-                     : "memory");
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(q_full);
-    }
-
-    const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of scaled logits (log2 units)
-    float l = 0.f;        // running sum of 2^(logit - m)
-    bool ok = true;
-
-    if (dump) {
-      ok = ptx::mbar_wait_warp(s_full, 0, limit, abort_flag);
-      if (ok && n > 0) {
+    if (tile_on && dump) {
+      if (ptx::mbar_wait_warp(s_full(t), 0, limit, abort_flag) && n > 0) {
         ptx::tc_fence_after();
-        float* dst = p.dump_scores + (int64_t(blockIdx.x) * 128 + r) * 128;
-#pragma unroll
+        float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
         for (int j = 0; j < 4; ++j) {
           uint32_t s[32];
-          ptx::tmem_ld32(tS + lane_off + 32 * j, s);
+          ptx::tmem_ld32(tS + 32 * j, s);
           ptx::tmem_wait_ld();
-#pragma unroll
           for (int e = 0; e < 32; ++e) dst[32 * j + e] = __uint_as_float(s[e]);
         }
       }
-    } else {
+    } else if (tile_on) {
+      float m = -INFINITY;  // running max of scaled logits (log2 units)
+      float l = 0.f;        // running sum of the bf16-rounded P
+      bool ok = true;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
-      for (int i = 0; i < n; ++i) {
+      for (int j = 0; j < n; ++j) {
         const int len = len_next;
-        if (i + 1 < n) len_next = __ldg(&p.chunks[c0 + i + 1].start_len) >> 16;
-        if (!(ok = ptx::mbar_wait_warp(s_full, i & 1, limit, abort_flag))) break;
+        if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
+        if (!(ok = ptx::mbar_wait_warp(s_full(t), j & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
-        if (warp_active) {
-          uint32_t s[128];
+        if (warp_on) {
+          // pass 1: row max over the 128 keys (two 64-column loads)
+          float mx = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t(&sj)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32 * j]);
-            ptx::tmem_ld32(tS + lane_off + 32 * j, sj);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t a[64];
+            uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[0]);
+            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[32]);
+            ptx::tmem_ld32(tS + 64 * hh, a0);
+            ptx::tmem_ld32(tS + 64 * hh + 32, a1);
+            ptx::tmem_wait_ld();
+            mx = max_masked32(a, 64 * hh, len, mx);
+            mx = max_masked32(a + 32, 64 * hh + 32, len, mx);
           }
-          ptx::tmem_wait_ld();
-          if (len < 128) {
-#pragma unroll
-            for (int j = 0; j < 128; ++j)
-              if (j >= len) s[j] = __float_as_uint(-INFINITY);
-          }
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 128; j += 4) {
-            mx0 = fmaxf(mx0, __uint_as_float(s[j]));
-            mx1 = fmaxf(mx1, __uint_as_float(s[j + 1]));
-            mx2 = fmaxf(mx2, __uint_as_float(s[j + 2]));
-            mx3 = fmaxf(mx3, __uint_as_float(s[j + 3]));
-          }
-          const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+          const float m_cand = mx * sl2;
           const bool need = m_cand > m + kRescaleThreshold;
           const float m_new = need ? m_cand : m;
-          if (i > 0 && __any_sync(0xffffffffu, need)) {
-            // O has PV of earlier chunks (complete: S of this chunk was issued after them)
+          if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // earlier PVs are complete: this chunk's S was issued after them
             const float corr = need ? ptx::ex2(m - m_new) : 1.f;
-#pragma unroll
-            for (int j = 0; j < D / 32; ++j) {
-              uint32_t o[32];
-              ptx::tmem_ld32(tO + lane_off + 32 * j, o);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-              ptx::tmem_st32(tO + lane_off + 32 * j, o);
-            }
+            rescale_tmem(tO, D, corr);
+            l *= corr;
           }
-          if (need) {
-            l *= ptx::ex2(m - m_new);
-            m = m_new;
-          }
+          m = m_new;
           const float neg_m = -m;
-          float sum0 = 0.f, sum1 = 0.f;
+          // pass 2: P = 2^(s - m) as bf16 over S; keys 64h..64h+63 -> packed columns 32h..32h+31,
+          // which only overwrite S columns already read
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e]), sl2, neg_m));
-              const float p1 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m));
-              sum0 += p0;
-              sum1 += p1;
-              pk[e] = pack_bf16(p0, p1);
-            }
-            ptx::tmem_st16(tS + lane_off + 16 * j, pk);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t a[64];
+            uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[0]);
+            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[32]);
+            ptx::tmem_ld32(tS + 64 * hh, a0);
+            ptx::tmem_ld32(tS + 64 * hh + 32, a1);
+            ptx::tmem_wait_ld();
+            mask32(a, 64 * hh, len);
+            mask32(a + 32, 64 * hh + 32, len);
+            l += exp_pack_store<64>(a, sl2, neg_m, tS + 32 * hh);
           }
           ptx::tmem_wait_st();
-          l += sum0 + sum1;
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(p_ready);
+        ptx::mbar_arrive(p_ready(t));
       }
       if (!ok) signal_abort(p.status, abort_flag);
-
-      // ---------------------------------------------------------- epilogue
-      if (ok && ptx::mbar_wait_warp(o_done, 0, limit, abort_flag) && warp_active) {
+      if (ok && ptx::mbar_wait_warp(o_done, 0, limit, abort_flag) && warp_on) {
         ptx::tc_fence_after();
         const float inv_l = 1.f / l;
-        if (work.nsplit == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (qrow * p.H + head) * D);
+#pragma unroll 1
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tO + 32 * j, v);
+          ptx::tmem_wait_ld();
+          if (row_ok) store_output_cols<D>(p, work, split, head, row, v, 32 * j, inv_l);
+        }
+        if (row_ok && work.nsplit > 1) p.part_lse[(int64_t(split) * p.H + head) * p.T + row] = m + __log2f(l);
+      }
+    }
+  } else if constexpr (C::kTail) {
+    // ------------------------------------------------------------ tail softmax (warps 0-3)
+    const int q = warp;                       // lane quarter = key group
+    const int i = lane;                       // tail row
+    const bool row_ok = has_tail && i < p.tail_rows;
+    const uint32_t lane_off = uint32_t(q * 32) << 16;
+    const uint32_t tS = tmem + C::kS2 + lane_off;
+    const uint32_t tO = tmem + C::kO2 + lane_off;
+    const int row = tail_row0 + i;
+    const int64_t qrow = int64_t(work.stream) * p.T + row;
+    if (has_tail)
+      store_q_row<D>(sQ2, q * 32 + i,
+                     reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D),
+                     row_ok);
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(q_full);
+    if (has_tail && !dump) {
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
+      for (int j = 0; ok && j < n; ++j) {
+        const int len = len_next;
+        if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
+        for (int h = 0; h < 2; ++h) {
+          if (!(ok = ptx::mbar_wait_warp(s_full(2), h, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          const int key0 = 64 * h + 16 * q;
+          uint32_t s[16];
+          ptx::tmem_ld16(tS + 16 * q, s);
+          ptx::tmem_wait_ld();
+          float mx = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + lane_off + 32 * j, o);
-            ptx::tmem_wait_ld();
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-            if (row_ok) {
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[4 * j + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
+          for (int e = 0; e < 16; ++e) {
+            if (key0 + e >= len) s[e] = __float_as_uint(-INFINITY);
+            mx = fmaxf(mx, __uint_as_float(s[e]));
           }
-        } else {
-          const int64_t idx = (int64_t(split) * p.H + head) * p.T + row;
-          float4* dst = reinterpret_cast<float4*>(p.part_o + idx * D);
-#pragma unroll
-          for (int j = 0; j < D / 32; ++j) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + lane_off + 32 * j, o);
-            ptx::tmem_wait_ld();
-            if (row_ok) {
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[8 * j + v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                             __uint_as_float(o[4 * v + 2]) * inv_l,
-                                             __uint_as_float(o[4 * v + 3]) * inv_l);
-            }
+          const float m_cand = mx * sl2;
+          const bool need = m_cand > m + kRescaleThreshold;
+          const float m_new = need ? m_cand : m;
+          if ((j > 0 || h > 0) && __any_sync(0xffffffffu, need)) {
+            const float corr = need ? ptx::ex2(m - m_new) : 1.f;
+            rescale_tmem(tO, 64, corr);
+            l *= corr;
           }
-          if (row_ok) p.part_lse[idx] = m + __log2f(l);
+          m = m_new;
+          const float neg_m = (m == -INFINITY) ? 0.f : -m;  // no key seen yet: every p is 0
+          uint32_t pk[8], zero[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            pk[e] = pack_bf16(ptx::ex2(fmaf(__uint_as_float(s[2 * e]), sl2, neg_m)),
+                              ptx::ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, neg_m)));
+            l += packed_sum(pk[e]);
+            zero[e] = 0u;
+          }
+          // this lane quarter's P is nonzero only on its own 16 keys (packed columns 8q..8q+7)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t(&src)[8] = (b == q) ? pk : zero;
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(tS + 8 * b),
+                "r"(src[0]), "r"(src[1]), "r"(src[2]), "r"(src[3]), "r"(src[4]), "r"(src[5]), "r"(src[6]),
+                "r"(src[7])
+                : "memory");
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(p_ready(2));
+        }
+      }
+      if (!ok) signal_abort(p.status, abort_flag);
+      // merge the four key-group partial states of every tail row
+      float* scratch = reinterpret_cast<float*>(smem + C::kKV);  // K/V stages are idle after o_done
+      float* sm = scratch + 4 * kTailMaxRows * 64;
+      float* sl = sm + 4 * kTailMaxRows;
+      const bool done = ok && ptx::mbar_wait_warp(o_done, 0, limit, abort_flag);
+      if (done) {
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tO + 32 * j, v);
+          ptx::tmem_wait_ld();
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(scratch + (q * kTailMaxRows + i) * 64 + 32 * j);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                   __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+          }
+        }
+        if (row_ok) {
+          sm[q * kTailMaxRows + i] = m;
+          sl[q * kTailMaxRows + i] = l;
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (done && !*abort_flag) {
+        for (int rr = q; rr < p.tail_rows; rr += 4) {
+          float mm = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) mm = fmaxf(mm, sm[g * kTailMaxRows + rr]);
+          float w[4], L = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            w[g] = exp2f(sm[g * kTailMaxRows + rr] - mm);
+            L += w[g] * sl[g * kTailMaxRows + rr];
+          }
+          float acc[2] = {0.f, 0.f};
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float* src = scratch + (g * kTailMaxRows + rr) * 64 + 2 * lane;
+            acc[0] += w[g] * src[0];
+            acc[1] += w[g] * src[1];
+          }
+          const float inv = 1.f / L;
+          const int orow = tail_row0 + rr;
+          if (work.nsplit == 1) {
+            const int64_t qr = int64_t(work.stream) * p.T + orow;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + (qr * p.H + head) * D);
+            dst[lane] = pack_bf16(acc[0] * inv, acc[1] * inv);
+          } else {
+            const int64_t idx = (int64_t(split) * p.H + head) * p.T + orow;
+            reinterpret_cast<float2*>(p.part_o + idx * D)[lane] = make_float2(acc[0] * inv, acc[1] * inv);
+            if (lane == 0) p.part_lse[idx] = mm + __log2f(L);
+          }
         }
       }
     }
@@ -352,13 +587,13 @@ __global__ void __launch_bounds__(kThreads, (D == 64) ? 2 : 1)
   __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, 512);
   }
 }
 
 template <int D>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t s) {
-  constexpr int smem = Smem<D>::kLaunchBytes;
+  constexpr int smem = Cfg<D>::kLaunch;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -368,7 +603,7 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int64_t grid = int64_t(p.num_splits) * p.H * p.ntiles;
+  const int64_t grid = int64_t(p.num_splits) * p.H * p.ngroups;
   if (grid <= 0 || grid > 0x7fffffff) return cudaErrorInvalidValue;
   attention_tc_kernel<D><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
   return cudaGetLastError();
@@ -380,6 +615,18 @@ cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map
   return p.D == 64 ? launch_tc<64>(p, kv_map, s) : launch_tc<128>(p, kv_map, s);
 }
 
-int attention_bf16_ctas_per_sm(int head_dim) { return head_dim == 64 ? 2 : 1; }
+TileShape attention_bf16_tiles(int T, int head_dim) {
+  TileShape ts{};
+  const int full = T / kTileRows, rem = T % kTileRows;
+  if (head_dim == 64 && rem > 0 && rem <= kTailMaxRows) {
+    ts.main_tiles = full;
+    ts.tail_rows = rem;
+  } else {
+    ts.main_tiles = full + (rem > 0 ? 1 : 0);
+    ts.tail_rows = 0;
+  }
+  ts.ngroups = ts.main_tiles > 0 ? (ts.main_tiles + 1) / 2 : 1;
+  return ts;
+}
 
 }  // namespace spk

@@ -234,27 +234,40 @@ int allocate_frame(spk_cache* c, StreamState& s) {
   return SPK_OK;
 }
 
+// KV splits per stream.  bf16: one CTA per SM and per (split, head, row group);
+// pick n minimising waves * (chunks per split + per-CTA overhead) + a small
+// charge per split for the partials it writes and the merge reads back.
 int choose_splits(const spk_cache* c, const std::vector<int32_t>& nchunks, std::vector<int32_t>& nsplit) {
   const spk_config& g = c->cfg;
   const int B = g.num_streams;
   nsplit.assign(B, 1);
-  int64_t total = 0;
-  for (int s = 0; s < B; ++s) total += nchunks[s];
   if (g.splits_per_stream > 0) {
     for (int s = 0; s < B; ++s)
       nsplit[s] = std::max(1, std::min({g.splits_per_stream, nchunks[s], kMaxSplitsPerStream}));
     return SPK_OK;
   }
-  const int ntiles = (c->T + kTileRows - 1) / kTileRows;
-  const int per_sm = g.dtype == SPK_BF16 ? attention_bf16_ctas_per_sm(g.head_dim) : 4;
-  const double slots = double(c->num_sms) * per_sm;
-  const double per_split = double(g.num_heads) * ntiles;
-  const double target = std::max(1.0, std::round(slots / per_split));
-  for (int s = 0; s < B; ++s) {
-    int n = int(std::lround(target * double(nchunks[s]) / double(std::max<int64_t>(total, 1))));
-    n = std::min(n, nchunks[s] / 2);  // at least two chunks per split
-    nsplit[s] = std::max(1, std::min(n, kMaxSplitsPerStream));
+  int32_t cmax = 0;
+  for (int s = 0; s < B; ++s) cmax = std::max(cmax, nchunks[s]);
+  int per_split_ctas, slots;
+  if (g.dtype == SPK_BF16) {
+    per_split_ctas = B * g.num_heads * attention_bf16_tiles(c->T, g.head_dim).ngroups;
+    slots = c->num_sms;
+  } else {
+    per_split_ctas = B * g.num_heads * ((c->T + 7) / 8);
+    slots = c->num_sms * 8;
   }
+  const double overhead_chunks = 2.0, split_charge = 0.25;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int n = 1; n <= std::min<int>(kMaxSplitsPerStream, std::max(1, cmax)); ++n) {
+    const double waves = std::ceil(double(per_split_ctas) * n / slots);
+    const double cost = waves * (std::ceil(double(cmax) / n) + overhead_chunks) + split_charge * n;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = n;
+    }
+  }
+  for (int s = 0; s < B; ++s) nsplit[s] = std::max(1, std::min(best, nchunks[s]));
   return SPK_OK;
 }
 
@@ -308,10 +321,10 @@ int build_plan(spk_cache* c) {
       c->works.push_back(WorkDesc{s, b0, b1, nsplit[s]});
     }
   }
-  const int ntiles = (c->T + kTileRows - 1) / kTileRows;
   c->info.num_chunks = int32_t(c->chunks.size());
   c->info.num_splits = int32_t(c->works.size());
-  c->info.num_ctas = int32_t(c->works.size()) * g.num_heads * ntiles;
+  c->info.num_ctas = int32_t(c->works.size()) * g.num_heads *
+                     (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->T, g.head_dim).ngroups : (c->T + 7) / 8);
   c->info.merge_needed = merge ? 1 : 0;
   c->info.visible_tokens = visible;
   return SPK_OK;
@@ -554,6 +567,12 @@ int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* 
   p.ps = g.page_size;
   p.num_splits = c->info.num_splits;
   p.ntiles = (c->T + kTileRows - 1) / kTileRows;
+  {
+    const TileShape ts = attention_bf16_tiles(c->T, g.head_dim);
+    p.main_tiles = ts.main_tiles;
+    p.tail_rows = ts.tail_rows;
+    p.ngroups = ts.ngroups;
+  }
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(g.head_dim)));
   p.wait_limit_ns = c->wait_limit_ns;
   p.dump_scores = dump_scores;

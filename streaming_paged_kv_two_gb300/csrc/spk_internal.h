@@ -86,7 +86,10 @@ struct AttnParams {
   int64_t half_stride;        // elements between K and V halves of a page (ps*H*D)
   int32_t T, H, D, ps;
   int32_t num_splits;
-  int32_t ntiles;             // query tiles of kTileRows per stream
+  int32_t ntiles;             // query tiles of kTileRows per stream (fp32 path)
+  int32_t main_tiles;         // bf16 path: 128-row query tiles handled by full warpgroups
+  int32_t tail_rows;          // bf16 path: trailing rows (<= 32) handled by the key-split tail warps
+  int32_t ngroups;            // bf16 path: CTAs per (split, head): pairs of main tiles, the tail on the last
   float scale_log2;           // log2(e) / sqrt(D)
   long long wait_limit_ns;
   float* dump_scores;         // diagnostics only: non-NULL makes the bf16 kernel write the raw
@@ -108,7 +111,12 @@ cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s);
 
-// Resident CTAs per SM the bf16 attention kernel is built for (planner input).
-int attention_bf16_ctas_per_sm(int head_dim);
+// Query-row tiling of the bf16 attention kernel for T rows and head_dim D.
+struct TileShape {
+  int main_tiles;
+  int tail_rows;
+  int ngroups;
+};
+TileShape attention_bf16_tiles(int T, int head_dim);
 
 }  // namespace spk
