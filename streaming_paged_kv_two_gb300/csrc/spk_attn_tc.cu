@@ -453,7 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok && work.nsplit > 1) p.part_lse[(int64_t(split) * p.H + head) * p.T + row] = m + __log2f(l);
       }
     }
-  } else if constexpr (C::kTail) {
+  } else if constexpr (!C::kTail) {
+    // warps 0-3 have no tail to work on; they still count towards q_full
+    ptx::mbar_arrive(q_full);
+  } else {
     // ------------------------------------------------------------ tail softmax (warps 0-3)
     const int q = warp;                       // lane quarter = key group
     const int i = lane;                       // tail row
