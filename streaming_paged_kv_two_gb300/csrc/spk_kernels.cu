@@ -49,54 +49,56 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
 // ------------------------------------------------------------------ merge
 // Exact recombination of softmax attention over disjoint key sets: with
 // M = max_j lse_j (log2 units) and w_j = 2^(lse_j - M),
-// out = sum_j w_j O_j / sum_j w_j.  One warp per (query row, head).
+// out = sum_j w_j O_j / sum_j w_j.  One thread per (query row, head, 4 columns); the
+// split loop is unrolled so the partial loads of several splits are in flight.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
-  constexpr int E = D / 32;  // elements per lane
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int rows = p.B * p.T;
-  if (warp >= rows * p.H) return;
-  const int row = warp / p.H;
-  const int h = warp - row * p.H;
+  constexpr int V = D / 4;  // float4 per row
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = int64_t(p.B) * p.T * p.H * V;
+  if (idx >= total) return;
+  const int c4 = int(idx % V);
+  const int64_t rh = idx / V;
+  const int h = int(rh % p.H);
+  const int row = int(rh / p.H);
   const int s = row / p.T;
   const int t = row - s * p.T;
   const StreamDesc sd = p.streams[s];
   if (sd.nsplit <= 1) return;  // written by the attention kernel
+  const int64_t base = (int64_t(sd.split_base) * p.H + h) * p.T + t;  // partial index of split 0
+  const int64_t step = int64_t(p.H) * p.T;                            // next split, same (head, row)
   float m = -INFINITY;
-  for (int j = 0; j < sd.nsplit; ++j) {
-    const float l = __ldg(&p.part_lse[(int64_t(sd.split_base + j) * p.H + h) * p.T + t]);
-    m = fmaxf(m, l);
-  }
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int j = 0; j < sd.nsplit; ++j) m = fmaxf(m, __ldg(&p.part_lse[base + j * step]));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
+#pragma unroll 4
   for (int j = 0; j < sd.nsplit; ++j) {
-    const int64_t idx = (int64_t(sd.split_base + j) * p.H + h) * p.T + t;
-    const float w = exp2f(__ldg(&p.part_lse[idx]) - m);
+    const int64_t pi = base + j * step;
+    const float w = exp2f(__ldg(&p.part_lse[pi]) - m);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + pi * D) + c4);
     wsum += w;
-    const float* o = p.part_o + idx * D + lane * E;
-    if constexpr (E == 2) {
-      const float2 v = __ldg(reinterpret_cast<const float2*>(o));
-      acc[0] += w * v.x; acc[1] += w * v.y;
-    } else {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(o));
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-    }
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
   const float inv = 1.f / wsum;
-  OutT* out = static_cast<OutT*>(p.out) + (int64_t(row) * p.H + h) * D + lane * E;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if constexpr (sizeof(OutT) == 2) out[e] = __float2bfloat16_rn(acc[e] * inv);
-    else out[e] = acc[e] * inv;
+  OutT* out = static_cast<OutT*>(p.out) + (int64_t(row) * p.H + h) * D + 4 * c4;
+  if constexpr (sizeof(OutT) == 2) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&a);
+    pk.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(out) = pk;
+  } else {
+    *reinterpret_cast<float4*>(out) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
 }
 
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s) {
-  const int64_t warps = int64_t(p.B) * p.T * p.H;
-  const int blocks = int((warps * 32 + 255) / 256);
+  const int64_t threads = int64_t(p.B) * p.T * p.H * (p.D / 4);
+  const int blocks = int((threads + 255) / 256);
   if (dtype == 0) {
     if (p.D == 64) merge_kernel<64, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
     else merge_kernel<128, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
