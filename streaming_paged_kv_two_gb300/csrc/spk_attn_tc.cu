@@ -158,6 +158,30 @@ __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float co
   }
 }
 
+// Scale the bf16 pairs in packed TMEM columns [0, ncols) of this warp's lanes by corr.
+__device__ __forceinline__ void rescale_packed_p(uint32_t taddr, int ncols, float corr) {
+  for (int j = 0; j < ncols; j += 16) {
+    uint32_t v[16];
+    ptx::tmem_ld16(taddr + j, v);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      v[e] = pack_bf16(__uint_as_float(v[e] << 16) * corr, __uint_as_float(v[e] & 0xFFFF0000u) * corr);
+    ptx::tmem_st16(taddr + j, v);
+  }
+}
+
+// Rare path of the online softmax (kept out of line so the hot loop's registers are
+// not spent on it): scale the first o_cols columns of O and the first p_cols packed
+// P columns of this chunk by corr.
+__device__ __noinline__ void rescale_running(uint32_t tO, uint32_t tS, int o_cols, int p_cols, float corr) {
+  if (o_cols) rescale_tmem(tO, o_cols, corr);
+  if (p_cols) {
+    ptx::tmem_wait_st();
+    rescale_packed_p(tS, p_cols, corr);
+  }
+}
+
 // Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
 // `scale`: bf16 output when the stream has one split, else the fp32 partial.
 template <int D>
@@ -292,62 +316,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_ts(o_tmem, p_tmem + 8 * k, ptx::smem_desc_sw128(sv + k * 2048, kColBlockBytes, 1024), idesc_pv,
                       (overwrite && k == 0) ? 0u : 1u);
       };
-      int full_seen = -1;
-      auto ensure_full = [&](int j) -> bool {
-        if (j <= full_seen) return true;
-        if (!ptx::mbar_wait_bounded(full_bar(j % S), (j / S) & 1, limit, abort_flag)) return false;
-        ptx::tc_fence_after();
-        full_seen = j;
-        return true;
-      };
-      const bool t0 = n_main >= 1, t1 = n_main >= 2;
+      // Event loop: three consumers (main tiles 0 and 1, the tail) each alternate
+      // "S issued, waiting for P" and "P ready: issue PV, then the next QK".  The loop
+      // services whichever consumer is ready, so no consumer waits behind another.
+      // A K/V stage is released once every consumer has issued its PV for that chunk.
+      const int ncons = n_main + (has_tail ? 1 : 0);
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
-      if (ok && n > 0 && (ok = ensure_full(0))) {
-        if (t0) { qk(tmem + C::kS0, sQ0, sK(0), idesc_qk); ptx::mma_commit(s_full(0)); }
-        if (t1) { qk(tmem + C::kS1, sQ1, sK(0), idesc_qk); ptx::mma_commit(s_full(1)); }
-        if (has_tail) { qk(tmem + C::kS2, sQ2, sK(0), idesc_qk_half); ptx::mma_commit(s_full(2)); }
+      int full_seen = -1;
+      auto full_ready = [&](int c) -> bool {
+        if (c <= full_seen) return true;
+        if (!ptx::mbar_test_wait(full_bar(c % S), (c / S) & 1)) return false;
+        ptx::tc_fence_after();
+        full_seen = c;
+        return true;
+      };
+      bool active[3] = {n_main >= 1, n_main >= 2, has_tail};
+      bool waiting[3] = {false, false, false};  // S issued, P not yet consumed
+      int cur[3] = {0, 0, 0};                   // chunk of the pending S / next QK
+      int half = 0;                             // tail: 64-key half of cur[2]
+      uint32_t pv_left = 0;                     // per stage, 8 bits: consumers yet to finish the chunk
+      for (int st = 0; st < S; ++st) pv_left |= uint32_t(ncons) << (8 * st);
+      if (dump) {
+        if (ok && n > 0) {
+          ok = ptx::mbar_wait_bounded(full_bar(0), 0, limit, abort_flag);
+          ptx::tc_fence_after();
+          if (ok && active[0]) { qk(tmem + C::kS0, sQ0, sK(0), idesc_qk); ptx::mma_commit(s_full(0)); }
+          if (ok && active[1]) { qk(tmem + C::kS1, sQ1, sK(0), idesc_qk); ptx::mma_commit(s_full(1)); }
+        }
+        for (int t = 0; t < 3; ++t) active[t] = false;
       }
-      for (int j = 0; ok && !dump && j < n; ++j) {
-        const int st = j % S;
-        const bool more = j + 1 < n;
-        const int nst = (j + 1) % S;
-        if (t0) {
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(0), j & 1, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          pv(tmem + C::kO0, tmem + C::kS0, sV(st), 8, j == 0);
-          if (more) {
-            if (!(ok = ensure_full(j + 1))) break;
-            qk(tmem + C::kS0, sQ0, sK(nst), idesc_qk);
-            ptx::mma_commit(s_full(0));
+      if (n == 0)
+        for (int t = 0; t < 3; ++t) active[t] = false;
+      long long idle_since = 0;
+      int idle = 0;
+      while (ok) {
+        bool any = false, progress = false;
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          if (!active[t]) continue;
+          any = true;
+          const uint32_t tS = tmem + (t == 0 ? C::kS0 : t == 1 ? C::kS1 : C::kS2);
+          const uint32_t sQ = t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2;
+          if (!waiting[t]) {
+            if (full_ready(cur[t])) {
+              qk(tS, sQ, sK(cur[t] % S), t < 2 ? idesc_qk : idesc_qk_half);
+              ptx::mma_commit(s_full(t));
+              waiting[t] = true;
+              half = t == 2 ? 0 : half;
+              progress = true;
+            }
+            continue;
           }
-        }
-        if (t1) {
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(1), j & 1, limit, abort_flag))) break;
+          const uint32_t parity = t < 2 ? uint32_t(cur[t] & 1) : uint32_t(half);
+          if (!ptx::mbar_test_wait(p_ready(t), parity)) continue;
           ptx::tc_fence_after();
-          pv(tmem + C::kO1, tmem + C::kS1, sV(st), 8, j == 0);
-          if (more) {
-            if (!(ok = ensure_full(j + 1))) break;
-            qk(tmem + C::kS1, sQ1, sK(nst), idesc_qk);
-            ptx::mma_commit(s_full(1));
-          }
-        }
-        if (has_tail) {
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 0, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          pv(tmem + C::kO2, tmem + C::kS2, sV(st), 4, j == 0);                 // keys 0..63
-          qk(tmem + C::kS2, sQ2, sK(st) + 64 * 128, idesc_qk_half);            // keys 64..127
-          ptx::mma_commit(s_full(2));
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 1, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          pv(tmem + C::kO2, tmem + C::kS2, sV(st) + 64 * 128, 4, false);
-          if (more) {
-            if (!(ok = ensure_full(j + 1))) break;
-            qk(tmem + C::kS2, sQ2, sK(nst), idesc_qk_half);
+          progress = true;
+          const int c = cur[t], st = c % S;
+          if (t < 2) {
+            pv(tmem + (t ? C::kO1 : C::kO0), tS, sV(st), 8, c == 0);
+          } else if (half == 0) {
+            pv(tmem + C::kO2, tS, sV(st), 4, c == 0);                 // keys 0..63
+            qk(tS, sQ, sK(st) + 64 * 128, idesc_qk_half);             // keys 64..127
             ptx::mma_commit(s_full(2));
+            half = 1;
+            continue;
+          } else {
+            pv(tmem + C::kO2, tS, sV(st) + 64 * 128, 4, false);
+          }
+          waiting[t] = false;
+          cur[t] = c + 1;
+          if (c + 1 == n) active[t] = false;
+          const uint32_t left = ((pv_left >> (8 * st)) & 0xFFu) - 1u;
+          if (left == 0) {
+            ptx::mma_commit(empty_bar(st));  // every consumer is done with this K/V stage
+            pv_left = (pv_left & ~(0xFFu << (8 * st))) | (uint32_t(ncons) << (8 * st));
+          } else {
+            pv_left = (pv_left & ~(0xFFu << (8 * st))) | (left << (8 * st));
           }
         }
-        ptx::mma_commit(empty_bar(st));
+        if (!any) break;
+        if (progress) {
+          idle = 0;
+        } else if (++idle == 64) {
+          idle_since = ptx::globaltimer_ns();
+        } else if (idle > 64 && (idle & 255) == 0) {
+          if (*abort_flag || ptx::globaltimer_ns() - idle_since > limit) ok = false;
+        }
       }
       if (!ok) signal_abort(p.status, abort_flag);
       ptx::mma_commit(o_done);  // arrives once every MMA issued above has completed
@@ -396,44 +451,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ptx::mbar_wait_warp(s_full(t), j & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
         if (warp_on) {
-          // pass 1: row max over the 128 keys (two 64-column loads)
-          float mx = -INFINITY;
+          // One pass over S in 32-column quarters; the next quarter's TMEM load is in
+          // flight while this one is exponentiated.  The running max m only moves when
+          // a quarter's max exceeds it by more than 2^8; then O (earlier chunks), the
+          // P already written for this chunk and l are rescaled, so every P of the
+          // chunk shares one offset.  P of keys 32k..32k+31 goes to packed columns
+          // 16k..16k+15, which only overwrite S columns already read.
+          uint32_t qa[32], qb[32];
+          ptx::tmem_ld32(tS, qa);
+          ptx::tmem_wait_ld();
+          auto quarter = [&](const int k, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+            if (k < 3) ptx::tmem_ld32(tS + 32 * (k + 1), nxt);
+            mask32(cur, 32 * k, len);
+            float mx = -INFINITY;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t a[64];
-            uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[0]);
-            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[32]);
-            ptx::tmem_ld32(tS + 64 * hh, a0);
-            ptx::tmem_ld32(tS + 64 * hh + 32, a1);
-            ptx::tmem_wait_ld();
-            mx = max_masked32(a, 64 * hh, len, mx);
-            mx = max_masked32(a + 32, 64 * hh + 32, len, mx);
-          }
-          const float m_cand = mx * sl2;
-          const bool need = m_cand > m + kRescaleThreshold;
-          const float m_new = need ? m_cand : m;
-          if (j > 0 && __any_sync(0xffffffffu, need)) {
-            // earlier PVs are complete: this chunk's S was issued after them
-            const float corr = need ? ptx::ex2(m - m_new) : 1.f;
-            rescale_tmem(tO, D, corr);
-            l *= corr;
-          }
-          m = m_new;
-          const float neg_m = -m;
-          // pass 2: P = 2^(s - m) as bf16 over S; keys 64h..64h+63 -> packed columns 32h..32h+31,
-          // which only overwrite S columns already read
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t a[64];
-            uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[0]);
-            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&a[32]);
-            ptx::tmem_ld32(tS + 64 * hh, a0);
-            ptx::tmem_ld32(tS + 64 * hh + 32, a1);
-            ptx::tmem_wait_ld();
-            mask32(a, 64 * hh, len);
-            mask32(a + 32, 64 * hh + 32, len);
-            l += exp_pack_store<64>(a, sl2, neg_m, tS + 32 * hh);
-          }
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(cur[e]));
+            const float m_cand = mx * sl2;
+            const bool need = m_cand > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, need)) {
+              const float m_new = need ? m_cand : m;
+              const float corr = need ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
+              rescale_running(tO, tS, j > 0 ? D : 0, 16 * k, corr);
+              l *= corr;
+              m = m_new;
+            }
+            l += exp_pack_store<32>(cur, sl2, -m, tS + 16 * k);
+            if (k < 3) ptx::tmem_wait_ld();
+          };
+          quarter(0, qa, qb);
+          quarter(1, qb, qa);
+          quarter(2, qa, qb);
+          quarter(3, qb, qa);
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
