@@ -274,7 +274,7 @@ def run_gpu(args, w: wl.Workload):
     total_frames = w.frames
     extra = W + K + 2                       # the e2e pass streams past the steady-state frame
     wk = w.replace(frames=total_frames + extra)
-    cfg, keep = spk_config_for(wk)
+    cfg, keep = spk_config_for(wk, args.splits)
     pool_bytes, ws_bytes = spk.required_bytes(cfg)
     dev = torch.device("cuda", local)
     pools = [torch.empty(pool_bytes, dtype=torch.uint8, device=dev) for _ in range(w.num_blocks)]
@@ -473,6 +473,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="tuning only: force this many KV splits per stream (0 = the planner's choice)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="profiling only: override the block count (smaller device footprint)")
     args = ap.parse_args(argv)

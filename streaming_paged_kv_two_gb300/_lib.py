@@ -82,6 +82,7 @@ def _load():
         "spk_read_device_status": (I32, [P, P, pi32]),
         "spk_selftest_wait_timeout": (I32, [P, I64, P]),
         "spk_debug_dump_scores": (I32, [P, I32, P, P, P, P]),
+        "spk_debug_trace_attention": (I32, [P, I32, P, P, P, P, ctypes.c_int32, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -199,6 +200,10 @@ class Cache:
 
     def debug_dump_scores(self, block: int, q, dst, workspace, cuda_stream=None):
         _check(lib.spk_debug_dump_scores(self._h, block, _ptr(q), _ptr(dst), _ptr(workspace), _stream(cuda_stream)))
+
+    def debug_trace_attention(self, block: int, q, out, workspace, trace, capacity: int, cuda_stream=None):
+        _check(lib.spk_debug_trace_attention(self._h, block, _ptr(q), _ptr(out), _ptr(workspace), _ptr(trace),
+                                             int(capacity), _stream(cuda_stream)))
 
     def read_kv(self, block: int, page_id: int, dst, cuda_stream=None):
         _check(lib.spk_read_kv(self._h, block, page_id, _ptr(dst), _stream(cuda_stream)))

@@ -74,6 +74,12 @@ struct Cfg {
   static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
 };
 
+// Trace mode (diagnostics): CTA 0 records the SM clock of an event for a chunk.
+__device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) {
+  if (p.trace != nullptr && blockIdx.x == 0 && chunk < p.trace_cap)
+    p.trace[int64_t(ev) * p.trace_cap + chunk] = clock64();
+}
+
 __device__ __forceinline__ void signal_abort(int32_t* status, volatile int* abort_flag) {
   *abort_flag = 1;
   atomicExch(status, kStatusWaitTimeout);
@@ -105,37 +111,36 @@ __device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src
 }
 
 // p = 2^(s*sl2 - m) for N fp32 scores in registers, packed to bf16 pairs and stored to
-// TMEM at column `dst`; returns the fp32 sum of the rounded values.
+// TMEM at column `dst`; returns the fp32 sum of the rounded values.  The argument is
+// one packed fp32x2 FMA per pair and the sum adds the two bf16 halves directly.
 template <int N>
 __device__ __forceinline__ float exp_pack_store(const uint32_t* s, float sl2, float neg_m, uint32_t dst) {
   static_assert(N % 32 == 0, "");
-  float sum0 = 0.f, sum1 = 0.f;
+  float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < N / 32; ++j) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float p0 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e]), sl2, neg_m));
-      const float p1 = ptx::ex2(fmaf(__uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m));
-      pk[e] = pack_bf16(p0, p1);
-      if (e & 1) sum1 += packed_sum(pk[e]);
-      else sum0 += packed_sum(pk[e]);
+      float x0, x1;
+      ptx::fma2(x0, x1, __uint_as_float(s[32 * j + 2 * e]), __uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m);
+      pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
+      sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
     }
     ptx::tmem_st16(dst + 16 * j, pk);
   }
-  return sum0 + sum1;
+  return (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
 
-__device__ __forceinline__ float max_masked32(const uint32_t* s, int first_key, int len, float mx) {
-  if (first_key + 32 <= len) {
+// max over 32 scores (three-input max: two new values per instruction)
+__device__ __forceinline__ float max32(const uint32_t* s, float mx) {
+  float a = mx, b = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(s[e]));
-  } else {
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (first_key + e < len) mx = fmaxf(mx, __uint_as_float(s[e]));
+  for (int e = 0; e < 32; e += 4) {
+    a = ptx::max3(a, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+    b = ptx::max3(b, __uint_as_float(s[e + 2]), __uint_as_float(s[e + 3]));
   }
-  return mx;
+  return fmaxf(a, b);
 }
 
 __device__ __forceinline__ void mask32(uint32_t* s, int first_key, int len) {
@@ -285,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ChunkDesc cd = p.chunks[c0 + i];
         const int start = cd.start_len & 0xFFFF;
         ptx::mbar_arrive_expect_tx(full_bar(st), 2 * C::kTile);
+        trace(p, kTrTmaIssue, i);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
           ptx::tma_load_4d(sK(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page, full_bar(st));
@@ -329,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_test_wait(full_bar(c % S), (c / S) & 1)) return false;
         ptx::tc_fence_after();
         full_seen = c;
+        trace(p, kTrFullSeen, c);
         return true;
       };
       bool active[3] = {n_main >= 1, n_main >= 2, has_tail};
@@ -362,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (full_ready(cur[t])) {
               qk(tS, sQ, sK(cur[t] % S), t < 2 ? idesc_qk : idesc_qk_half);
               ptx::mma_commit(s_full(t));
+              trace(p, t == 0 ? kTrQk0 : t == 1 ? kTrQk1 : kTrQk2a, cur[t]);
               waiting[t] = true;
               half = t == 2 ? 0 : half;
               progress = true;
@@ -373,12 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           progress = true;
           const int c = cur[t], st = c % S;
+          trace(p, t == 0 ? kTrP0Seen : t == 1 ? kTrP1Seen : (half == 0 ? kTrP2aSeen : kTrP2bSeen), c);
           if (t < 2) {
             pv(tmem + (t ? C::kO1 : C::kO0), tS, sV(st), 8, c == 0);
           } else if (half == 0) {
             pv(tmem + C::kO2, tS, sV(st), 4, c == 0);                 // keys 0..63
             qk(tS, sQ, sK(st) + 64 * 128, idesc_qk_half);             // keys 64..127
             ptx::mma_commit(s_full(2));
+            trace(p, kTrQk2b, c);
             half = 1;
             continue;
           } else {
@@ -390,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t left = ((pv_left >> (8 * st)) & 0xFFu) - 1u;
           if (left == 0) {
             ptx::mma_commit(empty_bar(st));  // every consumer is done with this K/V stage
+            trace(p, kTrEmpty, c);
             pv_left = (pv_left & ~(0xFFu << (8 * st))) | (uint32_t(ncons) << (8 * st));
           } else {
             pv_left = (pv_left & ~(0xFFu << (8 * st))) | (left << (8 * st));
@@ -450,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
         if (!(ok = ptx::mbar_wait_warp(s_full(t), j & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
+        if (q4 == 0 && lane == 0) trace(p, t ? kTrS1Seen : kTrS0Seen, j);
         if (warp_on) {
           // One pass over S in 32-column quarters; the next quarter's TMEM load is in
           // flight while this one is exponentiated.  The running max m only moves when
@@ -463,10 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto quarter = [&](const int k, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
             if (k < 3) ptx::tmem_ld32(tS + 32 * (k + 1), nxt);
             mask32(cur, 32 * k, len);
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(cur[e]));
-            const float m_cand = mx * sl2;
+            const float m_cand = max32(cur, -INFINITY) * sl2;
             const bool need = m_cand > m + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
               const float m_new = need ? m_cand : m;
@@ -485,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
+        if (q4 == 0 && lane == 0) trace(p, t ? kTrP1Arrive : kTrP0Arrive, j);
         ptx::mbar_arrive(p_ready(t));
       }
       if (!ok) signal_abort(p.status, abort_flag);
@@ -530,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           if (!(ok = ptx::mbar_wait_warp(s_full(2), h, limit, abort_flag))) break;
           ptx::tc_fence_after();
+          if (q == 0 && lane == 0) trace(p, h ? kTrS2bSeen : kTrS2aSeen, j);
           const int key0 = 64 * h + 16 * q;
           uint32_t s[16];
           ptx::tmem_ld16(tS + 16 * q, s);
@@ -570,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
+          if (q == 0 && lane == 0) trace(p, h ? kTrP2bArrive : kTrP2aArrive, j);
           ptx::mbar_arrive(p_ready(2));
         }
       }

@@ -532,7 +532,7 @@ int spk_plan(spk_cache* c, void* workspace, void* cuda_stream) {
 namespace {
 
 int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* workspace, void* cuda_stream,
-                       float* dump_scores) {
+                       float* dump_scores, unsigned long long* trace = nullptr, int32_t trace_cap = 0) {
   int rc = check_cache(c);
   if (rc) return rc;
   const spk_config& g = c->cfg;
@@ -576,6 +576,8 @@ int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* 
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(g.head_dim)));
   p.wait_limit_ns = c->wait_limit_ns;
   p.dump_scores = dump_scores;
+  p.trace = trace;
+  p.trace_cap = trace_cap;
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   cudaError_t e = g.dtype == SPK_BF16 ? launch_attention_bf16(p, &c->maps[block], stream)
                                       : launch_attention_f32(p, stream);
@@ -607,6 +609,14 @@ int spk_run_attention(spk_cache* c, int block, const void* q, void* out, void* w
 int spk_debug_dump_scores(spk_cache* c, int block, const void* q, float* dst, void* workspace, void* cuda_stream) {
   if (!dst) return fail(SPK_ERR_INVALID_ARG, "dst is NULL");
   return run_attention_impl(c, block, q, nullptr, workspace, cuda_stream, dst);
+}
+
+int spk_debug_trace_attention(spk_cache* c, int block, const void* q, void* out, void* workspace,
+                              uint64_t* trace, int32_t capacity, void* cuda_stream) {
+  if (!trace || capacity < 1) return fail(SPK_ERR_INVALID_ARG, "trace buffer is NULL or empty");
+  if (c && c->cfg.dtype != SPK_BF16) return fail(SPK_ERR_INVALID_ARG, "trace exists for the bf16 kernel only");
+  return run_attention_impl(c, block, q, out, workspace, cuda_stream, nullptr,
+                            reinterpret_cast<unsigned long long*>(trace), capacity);
 }
 
 int spk_read_kv(spk_cache* c, int block, int page_id, void* dst, void* cuda_stream) {

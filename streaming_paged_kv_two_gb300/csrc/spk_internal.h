@@ -18,6 +18,12 @@ constexpr int kMaxSplitsPerStream = 32;
 constexpr int kMaxSpecials = 64;
 // Query rows per tensor-core tile (tcgen05 M).
 constexpr int kTileRows = 128;
+// Events recorded by the bf16 attention kernel's trace mode (per chunk, CTA 0).
+enum TraceEvent {
+  kTrTmaIssue = 0, kTrFullSeen, kTrQk0, kTrP0Seen, kTrQk1, kTrP1Seen, kTrQk2a, kTrP2aSeen, kTrQk2b, kTrP2bSeen,
+  kTrEmpty, kTrS0Seen, kTrP0Arrive, kTrS1Seen, kTrP1Arrive, kTrS2aSeen, kTrP2aArrive, kTrS2bSeen, kTrP2bArrive,
+  kTraceEvents
+};
 // Device status word codes (first int32 of the workspace).
 constexpr int kStatusOk = 0;
 constexpr int kStatusWaitTimeout = 1;
@@ -92,6 +98,8 @@ struct AttnParams {
   int32_t ngroups;            // bf16 path: CTAs per (split, head): pairs of main tiles, the tail on the last
   float scale_log2;           // log2(e) / sqrt(D)
   long long wait_limit_ns;
+  unsigned long long* trace;  // diagnostics only: non-NULL makes CTA 0 record event clocks [kTraceEvents][trace_cap]
+  int32_t trace_cap;
   float* dump_scores;         // diagnostics only: non-NULL makes the bf16 kernel write the raw
                               // Q K^T tile of each CTA's first chunk ([ctas][128][128] fp32) and stop
 };
