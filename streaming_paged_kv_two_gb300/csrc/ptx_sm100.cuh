@@ -69,7 +69,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // (abort may be NULL: then only the time limit ends the wait).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns,
                                                   const volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = globaltimer_ns();
   for (;;) {
     for (int i = 0; i < 32; ++i)
@@ -80,13 +81,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Warp-uniform bounded wait: every lane polls, the verdict is the same on all lanes.
+// The clock is read only once the phase has not completed after a few polls.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, long long limit_ns,
                                                const volatile int* abort) {
+  for (int it = 0; it < 16; ++it)
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const long long t0 = globaltimer_ns();
   for (int it = 0;; ++it) {
-    const bool done = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    if ((it & 31) == 31) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if ((it & 15) == 15) {
       int give_up = (abort && *abort != 0) || (globaltimer_ns() - t0 > limit_ns);
       give_up = __shfl_sync(0xffffffffu, give_up, 0);
       if (give_up) return false;

@@ -409,10 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!any) break;
         if (progress) {
           idle = 0;
-        } else if (++idle == 64) {
-          idle_since = ptx::globaltimer_ns();
-        } else if (idle > 64 && (idle & 255) == 0) {
-          if (*abort_flag || ptx::globaltimer_ns() - idle_since > limit) ok = false;
+        } else {
+          ++idle;
+          if (idle > 8) __nanosleep(32);  // nothing ready: leave the issue slots to the softmax warps
+          if (idle == 64) {
+            idle_since = ptx::globaltimer_ns();
+          } else if (idle > 64 && (idle & 255) == 0) {
+            if (*abort_flag || ptx::globaltimer_ns() - idle_since > limit) ok = false;
+          }
         }
       }
       if (!ok) signal_abort(p.status, abort_flag);
