@@ -161,6 +161,27 @@ int spk_plan(spk_cache* cache, void* workspace, void* cuda_stream);
 int spk_run_attention(spk_cache* cache, int block, const void* q, void* out, void* workspace,
                       void* cuda_stream);
 
+/* The same attention as spk_run_attention, for callers that must not allocate device
+ * memory while they run: for example a real-time loop whose memory was fixed when it
+ * started, or a process in which another allocator already owns all device memory.
+ * spk_run_attention keeps each KV split's partial results in the caller's workspace;
+ * this call keeps them in a file-scope array inside the library instead
+ * (32 MiB per device, held by every device that loads the library until the
+ * process exits), so it needs nothing beyond its inputs and outputs and calls no
+ * allocator.  The plan tables are still read from `workspace`, the buffer given to
+ * spk_plan.  The pages describe no counterpart: this is a property of this
+ * library's interface only.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - A plan whose partials exceed the array (splits * H * T * (D + 1) * 4 bytes,
+ *     rounded up) returns SPK_ERR_INVALID_ARG; lower spk_config.splits_per_stream.
+ *   - Every call on a device shares the array and leaves its contents behind.
+ *     Nothing in it needs to start at zero: each partial is written before it is
+ *     read.  Calls whose GPU work overlaps (other streams, other caches) race on
+ *     the array; order them on one stream. */
+int spk_run_attention_static_scratch(spk_cache* cache, int block, const void* q, void* out, void* workspace,
+                                     void* cuda_stream);
+
 /* Copy one raw page [2, page_size, H, D] of block's pool to dst (host or device
  * memory, page_bytes = 2*ps*H*D*elem).  Synchronizes cuda_stream before returning. */
 int spk_read_kv(spk_cache* cache, int block, int page_id, void* dst, void* cuda_stream);

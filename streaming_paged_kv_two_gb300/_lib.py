@@ -81,6 +81,7 @@ def _load():
         "spk_get_stats": (I32, [P, I32, ctypes.POINTER(spk_stats)]),
         "spk_read_device_status": (I32, [P, P, pi32]),
         "spk_selftest_wait_timeout": (I32, [P, I64, P]),
+        "spk_run_attention_static_scratch": (I32, [P, I32, P, P, P, P]),
         "spk_debug_dump_scores": (I32, [P, I32, P, P, P, P]),
         "spk_debug_trace_attention": (I32, [P, I32, P, P, P, P, ctypes.c_int32, P]),
     }
@@ -197,6 +198,11 @@ class Cache:
 
     def run_attention(self, block: int, q, out, workspace, cuda_stream=None):
         _check(lib.spk_run_attention(self._h, block, _ptr(q), _ptr(out), _ptr(workspace), _stream(cuda_stream)))
+
+    def run_attention_static_scratch(self, block: int, q, out, workspace, cuda_stream=None):
+        """spk_run_attention with the split partials in the library's static device array."""
+        _check(lib.spk_run_attention_static_scratch(self._h, block, _ptr(q), _ptr(out), _ptr(workspace),
+                                                    _stream(cuda_stream)))
 
     def debug_dump_scores(self, block: int, q, dst, workspace, cuda_stream=None):
         _check(lib.spk_debug_dump_scores(self._h, block, _ptr(q), _ptr(dst), _ptr(workspace), _stream(cuda_stream)))

@@ -119,6 +119,11 @@ cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s);
 
+// Split-KV scratch in a file-scope device array (spk_static_scratch.cu): its size, and
+// its device address on the current device (resolved once per device).
+size_t static_scratch_bytes();
+cudaError_t static_scratch_address(void** out);
+
 // Query-row tiling of the bf16 attention kernel for T rows and head_dim D.
 struct TileShape {
   int main_tiles;
