@@ -13,7 +13,7 @@
 //
 // One CTA (one per SM) = (KV split, head, query-row group).  A group is up to two
 // 128-row "main" tiles, plus, on the last group when head_dim is 64, a "tail" of at
-// most 32 trailing rows (262 = 2 x 128 + 6).  Warp roles (14 warps):
+// most 32 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
 //   warps 0-3   tail softmax.  The tail's Q rows are replicated in the four TMEM
 //               lane quarters; warp q owns keys [16q, 16q+16) of every 64-key half
 //               chunk, so the tail's exponentials are spread evenly over the four
@@ -27,10 +27,12 @@
 //   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
 //               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
 //               swizzle, into a ring of shared-memory stages.
-//   warp 13     MMA issuer (one thread): S_t = Q_t K^T (M=128, N=128, K=D) and
-//               O_t += P_t V (M=128, N=D, K=128) per main tile, ping-ponged so one
-//               tile's MMAs run while the other tile's softmax runs; the tail
-//               works on 64-key halves (N=64, K=64).
+//   warps 13-15 MMA issuers, one thread per consumer (main tile 0, main tile 1,
+//               tail): S_t = Q_t K^T (M=128, N=128, K=D) and O_t += P_t V
+//               (M=128, N=D, K=128); the tail works on 64-key halves (N=64, K=64).
+//               The consumers advance independently, so one tile's MMAs run while
+//               the other tile's softmax runs; a K/V stage is released once every
+//               consumer is done with it.
 // TMEM (512 columns): S0 | S1 | O0 | O1 [| S2 (64) | O2 (64) when D = 64].
 // The epilogue writes bf16 output (one split) or an fp32 partial with its log2
 // log-sum-exp (several splits, combined by the merge kernel).
@@ -47,10 +49,10 @@ namespace {
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kTailMaxRows = 32;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
 constexpr int kWarpTma = 12;
-constexpr int kWarpMma = 13;
+constexpr int kWarpMma = 13;   // warps 13, 14, 15 issue the MMAs of main tile 0, main tile 1 and the tail
 constexpr int kSoftmaxThreads = 384;  // warps 0-11 (all arrive on q_full)
 
 template <int D>
@@ -64,7 +66,7 @@ struct Cfg {
   static constexpr int kKV = (kTail ? 3 : 2) * kTile;
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kBars = kKV + kStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kStages + 8;  // full, empty, q_full, s_full[3], p_ready[3], o_done
+  static constexpr int kNumBars = 2 * kStages + 10;  // full, empty, q_full, s_full[3], p_ready[3], o_done[3]
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_full = bars + 8 * (2 * S);
   auto s_full = [&](int t) { return q_full + 8 * (1 + t); };
   auto p_ready = [&](int t) { return q_full + 8 * (4 + t); };
-  const uint32_t o_done = q_full + 8 * 7;
+  auto o_done = [&](int t) { return q_full + 8 * (7 + t); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -252,16 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float sl2 = p.scale_log2;
 
   if (threadIdx.x == 0) {
+    const int ncons = max(1, n_main + (has_tail ? 1 : 0));
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(full_bar(i), 1);
-      ptx::mbar_init(empty_bar(i), 1);
+      ptx::mbar_init(empty_bar(i), ncons);  // one release per consumer of the chunk
     }
     ptx::mbar_init(q_full, kSoftmaxThreads);
     for (int t = 0; t < 3; ++t) {
       ptx::mbar_init(s_full(t), 1);
       ptx::mbar_init(p_ready(t), 128);
+      ptx::mbar_init(o_done(t), 1);
     }
-    ptx::mbar_init(o_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -303,125 +306,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, nullptr);
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp >= kWarpMma) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per consumer: warp 13 main tile 0, warp 14 main tile 1,
+    // warp 15 the tail.  Each runs its consumer's chain in order: wait for the K/V
+    // stage, S = Q K^T, commit; wait for P, O += P V, release the stage.  Shared-
+    // memory descriptors are built once; a k-step only adds to the address field.
+    const int t = warp - kWarpMma;
+    const bool mine = (t < 2) ? (t < n_main) : has_tail;
+    if (lane == 0 && mine) {
       constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t idesc_qk_half = ptx::idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
-      auto qk = [&](uint32_t d_tmem, uint32_t sq, uint32_t sk, uint32_t idesc) {
+      const uint32_t tS = tmem + (t == 0 ? C::kS0 : t == 1 ? C::kS1 : C::kS2);
+      const uint32_t tO = tmem + (t == 0 ? C::kO0 : t == 1 ? C::kO1 : C::kO2);
+      const uint64_t dQ = ptx::smem_desc_sw128(t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2, 16, 1024);
+      const uint64_t dK0 = ptx::smem_desc_sw128(sK(0), 16, 1024);
+      const uint64_t dV0 = ptx::smem_desc_sw128(sV(0), kColBlockBytes, 1024);
+      constexpr uint64_t kStageStep = C::kStageBytes >> 4;  // descriptor address units (16 bytes)
+      // S (+)= Q K^T over D: k-step k moves 32 bytes inside a 128-byte row, 16 KB per 64 columns
+      auto qk = [&](uint64_t dK, uint32_t idesc) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kColBlockBytes + (k & 3) * 32;
-          ptx::mma_ss(d_tmem, ptx::smem_desc_sw128(sq + off, 16, 1024), ptx::smem_desc_sw128(sk + off, 16, 1024),
-                      idesc, k > 0 ? 1u : 0u);
+          const uint64_t off = uint64_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+          ptx::mma_ss(tS, dQ + off, dK + off, idesc, k > 0 ? 1u : 0u);
         }
       };
-      auto pv = [&](uint32_t o_tmem, uint32_t p_tmem, uint32_t sv, int ksteps, bool overwrite) {
+      // O (+)= P V over `ksteps` x 16 keys starting at key row `row0`: a k-step is 16 rows (2 KB)
+      auto pv = [&](uint64_t dV, int key_row0, int ksteps, bool overwrite) {
         for (int k = 0; k < ksteps; ++k)
-          ptx::mma_ts(o_tmem, p_tmem + 8 * k, ptx::smem_desc_sw128(sv + k * 2048, kColBlockBytes, 1024), idesc_pv,
+          ptx::mma_ts(tO, tS + 8 * k, dV + uint64_t((key_row0 + 16 * k) * 8), idesc_pv,
                       (overwrite && k == 0) ? 0u : 1u);
       };
-      // Event loop: three consumers (main tiles 0 and 1, the tail) each alternate
-      // "S issued, waiting for P" and "P ready: issue PV, then the next QK".  The loop
-      // services whichever consumer is ready, so no consumer waits behind another.
-      // A K/V stage is released once every consumer has issued its PV for that chunk.
-      const int ncons = n_main + (has_tail ? 1 : 0);
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
-      int full_seen = -1;
-      auto full_ready = [&](int c) -> bool {
-        if (c <= full_seen) return true;
-        if (!ptx::mbar_test_wait(full_bar(c % S), (c / S) & 1)) return false;
+      const int nmma = dump ? (t < 2 ? min(n, 1) : 0) : n;
+      for (int c = 0; ok && c < nmma; ++c) {
+        const int st = c % S;
+        if (!(ok = ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
-        full_seen = c;
         trace(p, kTrFullSeen, c);
-        return true;
-      };
-      bool active[3] = {n_main >= 1, n_main >= 2, has_tail};
-      bool waiting[3] = {false, false, false};  // S issued, P not yet consumed
-      int cur[3] = {0, 0, 0};                   // chunk of the pending S / next QK
-      int half = 0;                             // tail: 64-key half of cur[2]
-      uint32_t pv_left = 0;                     // per stage, 8 bits: consumers yet to finish the chunk
-      for (int st = 0; st < S; ++st) pv_left |= uint32_t(ncons) << (8 * st);
-      if (dump) {
-        if (ok && n > 0) {
-          ok = ptx::mbar_wait_bounded(full_bar(0), 0, limit, abort_flag);
+        const uint64_t dK = dK0 + uint64_t(st) * kStageStep;
+        const uint64_t dV = dV0 + uint64_t(st) * kStageStep;
+        if (t < 2) {
+          qk(dK, idesc_qk);
+          ptx::mma_commit(s_full(t));
+          trace(p, t ? kTrQk1 : kTrQk0, c);
+          if (dump) break;
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(t), c & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
-          if (ok && active[0]) { qk(tmem + C::kS0, sQ0, sK(0), idesc_qk); ptx::mma_commit(s_full(0)); }
-          if (ok && active[1]) { qk(tmem + C::kS1, sQ1, sK(0), idesc_qk); ptx::mma_commit(s_full(1)); }
-        }
-        for (int t = 0; t < 3; ++t) active[t] = false;
-      }
-      if (n == 0)
-        for (int t = 0; t < 3; ++t) active[t] = false;
-      long long idle_since = 0;
-      int idle = 0;
-      while (ok) {
-        bool any = false, progress = false;
-#pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          if (!active[t]) continue;
-          any = true;
-          const uint32_t tS = tmem + (t == 0 ? C::kS0 : t == 1 ? C::kS1 : C::kS2);
-          const uint32_t sQ = t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2;
-          if (!waiting[t]) {
-            if (full_ready(cur[t])) {
-              qk(tS, sQ, sK(cur[t] % S), t < 2 ? idesc_qk : idesc_qk_half);
-              ptx::mma_commit(s_full(t));
-              trace(p, t == 0 ? kTrQk0 : t == 1 ? kTrQk1 : kTrQk2a, cur[t]);
-              waiting[t] = true;
-              half = t == 2 ? 0 : half;
-              progress = true;
-            }
-            continue;
-          }
-          const uint32_t parity = t < 2 ? uint32_t(cur[t] & 1) : uint32_t(half);
-          if (!ptx::mbar_test_wait(p_ready(t), parity)) continue;
-          ptx::tc_fence_after();
-          progress = true;
-          const int c = cur[t], st = c % S;
-          trace(p, t == 0 ? kTrP0Seen : t == 1 ? kTrP1Seen : (half == 0 ? kTrP2aSeen : kTrP2bSeen), c);
-          if (t < 2) {
-            pv(tmem + (t ? C::kO1 : C::kO0), tS, sV(st), 8, c == 0);
-          } else if (half == 0) {
-            pv(tmem + C::kO2, tS, sV(st), 4, c == 0);                 // keys 0..63
-            qk(tS, sQ, sK(st) + 64 * 128, idesc_qk_half);             // keys 64..127
-            ptx::mma_commit(s_full(2));
-            trace(p, kTrQk2b, c);
-            half = 1;
-            continue;
-          } else {
-            pv(tmem + C::kO2, tS, sV(st) + 64 * 128, 4, false);
-          }
-          waiting[t] = false;
-          cur[t] = c + 1;
-          if (c + 1 == n) active[t] = false;
-          const uint32_t left = ((pv_left >> (8 * st)) & 0xFFu) - 1u;
-          if (left == 0) {
-            ptx::mma_commit(empty_bar(st));  // every consumer is done with this K/V stage
-            trace(p, kTrEmpty, c);
-            pv_left = (pv_left & ~(0xFFu << (8 * st))) | (uint32_t(ncons) << (8 * st));
-          } else {
-            pv_left = (pv_left & ~(0xFFu << (8 * st))) | (left << (8 * st));
-          }
-        }
-        if (!any) break;
-        if (progress) {
-          idle = 0;
+          trace(p, t ? kTrP1Seen : kTrP0Seen, c);
+          pv(dV, 0, 8, c == 0);
         } else {
-          ++idle;
-          if (idle > 8) __nanosleep(32);  // nothing ready: leave the issue slots to the softmax warps
-          if (idle == 64) {
-            idle_since = ptx::globaltimer_ns();
-          } else if (idle > 64 && (idle & 255) == 0) {
-            if (*abort_flag || ptx::globaltimer_ns() - idle_since > limit) ok = false;
-          }
+          qk(dK, idesc_qk_half);                                  // keys 0..63
+          ptx::mma_commit(s_full(2));
+          trace(p, kTrQk2a, c);
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 0, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          trace(p, kTrP2aSeen, c);
+          pv(dV, 0, 4, c == 0);
+          qk(dK + uint64_t(64 * 128 >> 4), idesc_qk_half);        // keys 64..127
+          ptx::mma_commit(s_full(2));
+          trace(p, kTrQk2b, c);
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          trace(p, kTrP2bSeen, c);
+          pv(dV, 64, 4, false);
         }
+        ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
+        trace(p, kTrEmpty, c);
       }
       if (!ok) signal_abort(p.status, abort_flag);
-      ptx::mma_commit(o_done);  // arrives once every MMA issued above has completed
-      ptx::mbar_wait_bounded(o_done, 0, limit, nullptr);
+      ptx::mma_commit(o_done(t));  // arrives once every MMA this thread issued has completed
+      ptx::mbar_wait_bounded(o_done(t), 0, limit, nullptr);
     }
     __syncwarp();
   } else if (warp >= kWarpMain) {
@@ -502,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(p_ready(t));
       }
       if (!ok) signal_abort(p.status, abort_flag);
-      if (ok && ptx::mbar_wait_warp(o_done, 0, limit, abort_flag) && warp_on) {
+      if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
         ptx::tc_fence_after();
         const float inv_l = 1.f / l;
 #pragma unroll 1
@@ -591,10 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) signal_abort(p.status, abort_flag);
       // merge the four key-group partial states of every tail row
-      float* scratch = reinterpret_cast<float*>(smem + C::kKV);  // K/V stages are idle after o_done
+      float* scratch = reinterpret_cast<float*>(smem + C::kKV);  // K/V stages: see below
       float* sm = scratch + 4 * kTailMaxRows * 64;
       float* sl = sm + 4 * kTailMaxRows;
-      const bool done = ok && ptx::mbar_wait_warp(o_done, 0, limit, abort_flag);
+      const bool done = ok && ptx::mbar_wait_warp(o_done(2), 0, limit, abort_flag);
       if (done) {
         ptx::tc_fence_after();
 #pragma unroll 1
