@@ -548,10 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) signal_abort(p.status, abort_flag);
       // merge the four key-group partial states of every tail row
-      float* scratch = reinterpret_cast<float*>(smem + C::kKV);  // K/V stages: see below
+      // The merge scratch reuses the K/V stage ring, so it may be written only once every
+      // consumer's MMAs (and with them every load of this CTA) have completed.
+      float* scratch = reinterpret_cast<float*>(smem + C::kKV);
       float* sm = scratch + 4 * kTailMaxRows * 64;
       float* sl = sm + 4 * kTailMaxRows;
-      const bool done = ok && ptx::mbar_wait_warp(o_done(2), 0, limit, abort_flag);
+      bool done = ok;
+      for (int u = 0; u < 3 && done; ++u)
+        if (u == 2 || u < n_main) done = ptx::mbar_wait_warp(o_done(u), 0, limit, abort_flag);
       if (done) {
         ptx::tc_fence_after();
 #pragma unroll 1
