@@ -108,6 +108,35 @@ def block_work(w: wl.Workload, f: int):
     return 4.0 * t * n * h * d * b, (2.0 * n + 2.0 * t) * h * d * e * b
 
 
+# ---------------------------------------------------------------- ncu traffic record
+
+KERNEL_SOURCES = ("streaming_paged_kv_two_gb300/csrc/spk_attn_tc.cu", "streaming_paged_kv_two_gb300/csrc/ptx_sm100.cuh",
+                  "streaming_paged_kv_two_gb300/csrc/spk_internal.h", "streaming_paged_kv_two_gb300/csrc/spk_kernels.cu")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch (attention + merge kernels) from the committed ncu
+    record, or None when the record is missing, for another workload, or older than the
+    kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    if rec.get("source_hash") != kernel_source_hash() or rec.get("workload") != workload:
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -434,7 +463,7 @@ def run_gpu(args, w: wl.Workload):
                    "l2": "no flush: visible K/V per block exceeds L2",
                    "parallelism": f"replicas x{world} (independent streams, no data-path collective)"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "kernel": "attention (tcgen05 paged attention + LSE merge), per block launch",
                      "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
                      "avg_launch_us": avg_launch * 1e6, "algorithmic_bytes_per_launch": byts,

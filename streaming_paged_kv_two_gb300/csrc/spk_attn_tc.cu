@@ -304,6 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = issued > S ? issued - S : 0; i < issued; ++i)  // drain: copies must land before exit
         ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, nullptr);
+    } else if (lane == 1 && p.trace != nullptr && blockIdx.x == 0) {
+      // trace mode: watch the full barriers and record when each chunk's K/V lands
+      for (int i = 0; i < n; ++i)
+        if (ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, abort_flag)) trace(p, kTrLanded, i);
     }
     __syncwarp();
   } else if (warp >= kWarpMma) {

@@ -22,7 +22,7 @@ constexpr int kTileRows = 128;
 enum TraceEvent {
   kTrTmaIssue = 0, kTrFullSeen, kTrQk0, kTrP0Seen, kTrQk1, kTrP1Seen, kTrQk2a, kTrP2aSeen, kTrQk2b, kTrP2bSeen,
   kTrEmpty, kTrS0Seen, kTrP0Arrive, kTrS1Seen, kTrP1Arrive, kTrS2aSeen, kTrP2aArrive, kTrS2bSeen, kTrP2bArrive,
-  kTraceEvents
+  kTrLanded, kTraceEvents
 };
 // Device status word codes (first int32 of the workspace).
 constexpr int kStatusOk = 0;
