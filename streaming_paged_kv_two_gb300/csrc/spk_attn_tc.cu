@@ -43,6 +43,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 namespace spk {
 namespace {
 
@@ -324,24 +326,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
       const uint32_t tS = tmem + (t == 0 ? C::kS0 : t == 1 ? C::kS1 : C::kS2);
       const uint32_t tO = tmem + (t == 0 ? C::kO0 : t == 1 ? C::kO1 : C::kO2);
-      const uint64_t dQ = ptx::smem_desc_sw128(t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2, 16, 1024);
-      const uint64_t dK0 = ptx::smem_desc_sw128(sK(0), 16, 1024);
-      const uint64_t dV0 = ptx::smem_desc_sw128(sV(0), kColBlockBytes, 1024);
-      constexpr uint64_t kStageStep = C::kStageBytes >> 4;  // descriptor address units (16 bytes)
+      // Descriptors split into a constant high word (stride, version, 128-byte swizzle)
+      // and a low word (start address >> 4, leading offset); k-steps add constants.
+      const uint64_t dq = ptx::smem_desc_sw128(t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2, 16, 1024);
+      const uint32_t hi = uint32_t(dq >> 32);
+      const uint32_t q_lo = uint32_t(dq);
+      const uint32_t k0_lo = uint32_t(ptx::smem_desc_sw128(sK(0), 16, 1024));
+      const uint32_t v0_lo = uint32_t(ptx::smem_desc_sw128(sV(0), kColBlockBytes, 1024));
+      constexpr uint32_t kStageStep = C::kStageBytes >> 4;  // 16-byte units
       // S (+)= Q K^T over D: k-step k moves 32 bytes inside a 128-byte row, 16 KB per 64 columns
-      auto qk = [&](uint64_t dK, uint32_t idesc) {
+      auto qk = [&](uint32_t k_lo, uint32_t idesc) {
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t off = uint64_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
-          ptx::mma_ss(tS, dQ + off, dK + off, idesc, k > 0 ? 1u : 0u);
+          const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+          if (k == 0) ptx::mma_ss_lh<0>(tS, q_lo + off, k_lo + off, hi, idesc);
+          else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc);
         }
       };
-      // O (+)= P V over `ksteps` x 16 keys starting at key row `row0`: a k-step is 16 rows (2 KB)
-      auto pv = [&](uint64_t dV, int key_row0, int ksteps, bool overwrite) {
-        for (int k = 0; k < ksteps; ++k)
-          ptx::mma_ts(tO, tS + 8 * k, dV + uint64_t((key_row0 + 16 * k) * 8), idesc_pv,
-                      (overwrite && k == 0) ? 0u : 1u);
+      // O (+)= P V over KSTEPS x 16 keys: a k-step is 16 key rows (2 KB) of V and 8 TMEM columns of P
+      auto pv = [&](auto ksteps_tag, uint32_t v_lo, uint32_t p_col, uint32_t first_accumulate) {
+        constexpr int KSTEPS = decltype(ksteps_tag)::value;
+#pragma unroll
+        for (int k = 0; k < KSTEPS; ++k)
+          ptx::mma_ts_lh(tO, p_col + 8 * k, v_lo + uint32_t(128 * k), hi, idesc_pv, k == 0 ? first_accumulate : 1u);
       };
+      using K8 = std::integral_constant<int, 8>;
+      using K4 = std::integral_constant<int, 4>;
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
       const int nmma = dump ? (t < 2 ? min(n, 1) : 0) : n;
@@ -350,32 +360,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
         trace(p, kTrFullSeen, c);
-        const uint64_t dK = dK0 + uint64_t(st) * kStageStep;
-        const uint64_t dV = dV0 + uint64_t(st) * kStageStep;
+        const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
+        const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep;
+        const uint32_t acc0 = c > 0 ? 1u : 0u;
         if (t < 2) {
-          qk(dK, idesc_qk);
+          qk(k_lo, idesc_qk);
           ptx::mma_commit(s_full(t));
           trace(p, t ? kTrQk1 : kTrQk0, c);
           if (dump) break;
           if (!(ok = ptx::mbar_wait_bounded(p_ready(t), c & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace(p, t ? kTrP1Seen : kTrP0Seen, c);
-          pv(dV, 0, 8, c == 0);
+          pv(K8{}, v_lo, tS, acc0);
         } else {
-          qk(dK, idesc_qk_half);                                  // keys 0..63
+          qk(k_lo, idesc_qk_half);                                  // keys 0..63
           ptx::mma_commit(s_full(2));
           trace(p, kTrQk2a, c);
           if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 0, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace(p, kTrP2aSeen, c);
-          pv(dV, 0, 4, c == 0);
-          qk(dK + uint64_t(64 * 128 >> 4), idesc_qk_half);        // keys 64..127
+          pv(K4{}, v_lo, tS, acc0);
+          qk(k_lo + uint32_t(64 * 128 >> 4), idesc_qk_half);        // keys 64..127
           ptx::mma_commit(s_full(2));
           trace(p, kTrQk2b, c);
           if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace(p, kTrP2bSeen, c);
-          pv(dV, 64, 4, false);
+          pv(K4{}, v_lo + uint32_t(64 * 128 >> 4), tS, 1u);
         }
         ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
         trace(p, kTrEmpty, c);
