@@ -481,7 +481,9 @@ def run_gpu(args, w: wl.Workload):
         "fast_forward_s": t_ff,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        times, cpu_value = oracle_block_sample(w, f_first + K, heads=2, reps=50, budget_s=20.0)
+        reps = 50
+        times, cpu_value = oracle_block_sample(w.replace(frames=f_first + K + reps + 4), f_first + K, heads=2,
+                                               reps=reps, budget_s=20.0)
         line["cpu_baseline"] = {
             "value": cpu_value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": (f"{len(times)} reps of one frame of bookkeeping + gather + fp64 attention of block 0 over 2 "
