@@ -13,27 +13,32 @@
 //
 // One CTA (one per SM) = (KV split, head, query-row group).  A group is up to two
 // 128-row "main" tiles, plus, on the last group when head_dim is 64, a "tail" of at
-// most 32 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
-//   warps 0-3   tail softmax.  The tail's Q rows are replicated in the four TMEM
-//               lane quarters; warp q owns keys [16q, 16q+16) of every 64-key half
-//               chunk, so the tail's exponentials are spread evenly over the four
-//               SM sub-partitions.  Each warp keeps its own (max, sum, O) and the
-//               four partial states are merged at the end.
+// most 16 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
 //   warps 4-7   softmax of main tile 0, warps 8-11 softmax of main tile 1: one
-//               thread per query row (= TMEM lane).  fp32 online softmax in log2
-//               units, masking of the chunk's ragged tail, P written back as bf16
-//               over S, row sums taken from the rounded P that the MMA consumes,
-//               O rescaled in TMEM only when the running maximum grows by > 2^8.
+//               thread per query row (= TMEM lane).  Each tile has two 64-key score
+//               buffers in TMEM, so Q K^T of the next half chunk runs on the tensor
+//               core while the softmax works on the current one.  fp32 online
+//               softmax in log2 units, masking of the chunk's ragged tail, P written
+//               back as bf16 over S, row sums taken from the rounded P that the MMA
+//               consumes, O rescaled in TMEM only when the running maximum grows by
+//               more than 2^8.
+//   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
+//               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
+//               every tail row; warp q owns keys [32q, 32q+32) of each chunk and keeps
+//               its own (max, sum, O) per row.  Its P goes to a shared-memory tile in
+//               which the rows of key group q sit in TMEM lane quarter q, so one
+//               O2 += P2 V MMA accumulates the four partial states side by side; they
+//               are merged at the end.
 //   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
 //               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
 //               swizzle, into a ring of shared-memory stages.
 //   warps 13-15 MMA issuers, one thread per consumer (main tile 0, main tile 1,
-//               tail): S_t = Q_t K^T (M=128, N=128, K=D) and O_t += P_t V
-//               (M=128, N=D, K=128); the tail works on 64-key halves (N=64, K=64).
-//               The consumers advance independently, so one tile's MMAs run while
-//               the other tile's softmax runs; a K/V stage is released once every
-//               consumer is done with it.
-// TMEM (512 columns): S0 | S1 | O0 | O1 [| S2 (64) | O2 (64) when D = 64].
+//               tail).  Main tile t, half chunk g: S_t[g%2] = Q_t K_g^T (M=128, N=64,
+//               K=D), then, once the softmax has written P_g, O_t += P_g V_g (M=128,
+//               N=D, K=64) followed by Q K^T of half g+2 into the buffer just read.
+//               The consumers advance independently; a K/V stage is released once
+//               every consumer is done with it.
+// TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) | O0 | O1 [| O2 (64) | S2^T (16)].
 // The epilogue writes bf16 output (one split) or an fp32 partial with its log2
 // log-sum-exp (several splits, combined by the merge kernel).
 // Every wait is bounded: on timeout the kernel records a status word, drains its
@@ -50,7 +55,8 @@ namespace {
 
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kTailMaxRows = 32;
+constexpr int kTailMaxRows = 16;           // the N of the transposed tail MMA
+constexpr int kHalfKeys = 64;              // keys per main-tile score buffer
 constexpr int kThreads = 512;
 constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
 constexpr int kWarpTma = 12;
@@ -64,19 +70,26 @@ struct Cfg {
   static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kTile;
-  static constexpr int kQ2 = 2 * kTile;  // tail Q (D == 64)
-  static constexpr int kKV = (kTail ? 3 : 2) * kTile;
+  static constexpr int kQ2 = 2 * kTile;                 // tail Q: 16 rows x 128 bytes (D == 64)
+  static constexpr int kP2 = kQ2 + 2048;                // tail P: 128 rows x 128 keys bf16, two column blocks
+  static constexpr int kKV = kTail ? kP2 + 2 * kColBlockBytes : 2 * kTile;
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kBars = kKV + kStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kStages + 10;  // full, empty, q_full, s_full[3], p_ready[3], o_done[3]
+  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full, p2_ready
+  static constexpr int kNumBars = 2 * kStages + 16;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t kS0 = 0, kS1 = 128, kO0 = 256, kO1 = 256 + D;
-  static constexpr uint32_t kS2 = 256 + 2 * D, kO2 = 256 + 2 * D + 64;  // D == 64 only
-  static_assert(!kTail || kO2 + 64 <= 512, "TMEM budget");
+  static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + D;
+  static constexpr uint32_t kO2 = 4 * kHalfKeys + 2 * D, kS2 = kO2 + 64;  // D == 64 only
+  static_assert(kTail ? kS2 + kTailMaxRows <= 512 : kO1 + D <= 512, "TMEM budget");
+  static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
   static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
+  static_assert(kLaunch <= 227 * 1024, "shared memory per CTA");
 };
+
+// TMEM column of main tile t's score buffer b
+__device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(kHalfKeys * (2 * t + b)); }
 
 // Trace mode (diagnostics): CTA 0 records the SM clock of an event for a chunk.
 __device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) {
@@ -94,9 +107,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// sum of the two bf16 values held in a packed pair, in fp32
-__device__ __forceinline__ float packed_sum(uint32_t pk) {
-  return __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+// max over the 32 lanes of a warp
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Byte address of element (row, key) of the tail's P tile: 128 rows x 128 keys bf16,
+// K-major, 128-byte swizzle, keys 0-63 and 64-127 in two 16 KB column blocks.
+__device__ __forceinline__ uint32_t p2_addr(uint32_t base, int row, int key) {
+  return base + uint32_t((key >> 6) * kColBlockBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+                         ((((key & 63) >> 3) ^ (row & 7)) << 4) + (key & 7) * 2);
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
 // Store one row of a 128-row Q tile in K-major 128-byte-swizzled layout: 16-byte
@@ -181,14 +217,22 @@ __device__ __forceinline__ void rescale_packed_p(uint32_t taddr, int ncols, floa
 }
 
 // Rare path of the online softmax (kept out of line so the hot loop's registers are
-// not spent on it): scale the first o_cols columns of O and the first p_cols packed
-// P columns of this chunk by corr.
-__device__ __noinline__ void rescale_running(uint32_t tO, uint32_t tS, int o_cols, int p_cols, float corr) {
-  if (o_cols) rescale_tmem(tO, o_cols, corr);
-  if (p_cols) {
-    ptx::tmem_wait_st();
-    rescale_packed_p(tS, p_cols, corr);
+// not spent on it), taken at the end of a half chunk in which some row's running max
+// moved: wait until O holds every earlier PV (when o_cols > 0: the PV of the previous
+// half, tracked by pv_bar), scale the first o_cols columns of O by corr_o and the
+// half's first quarter of packed P (16 columns) by corr_p.  False when the wait gave up.
+__device__ __noinline__ bool rescale_running(uint32_t tO, uint32_t tS, int o_cols, float corr_o, float corr_p,
+                                             uint32_t pv_bar, uint32_t parity, long long limit,
+                                             const volatile int* abort_flag) {
+  bool ok = true;
+  if (o_cols) {
+    ok = ptx::mbar_wait_warp(pv_bar, parity, limit, abort_flag);
+    ptx::tc_fence_after();
+    rescale_tmem(tO, o_cols, corr_o);
   }
+  rescale_packed_p(tS, 16, corr_p);
+  ptx::tmem_wait_st();
+  return ok;
 }
 
 // Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
@@ -223,16 +267,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  const uint32_t sQ0 = sbase + C::kQ0, sQ1 = sbase + C::kQ1, sQ2 = sbase + C::kQ2;
+  const uint32_t sQ0 = sbase + C::kQ0, sQ1 = sbase + C::kQ1, sQ2 = sbase + C::kQ2, sP2 = sbase + C::kP2;
   auto sK = [&](int st) { return sbase + C::kKV + st * C::kStageBytes; };
   auto sV = [&](int st) { return sbase + C::kKV + st * C::kStageBytes + C::kTile; };
   const uint32_t bars = sbase + C::kBars;
   auto full_bar = [&](int st) { return bars + 8 * st; };
   auto empty_bar = [&](int st) { return bars + 8 * (S + st); };
   const uint32_t q_full = bars + 8 * (2 * S);
-  auto s_full = [&](int t) { return q_full + 8 * (1 + t); };
-  auto p_ready = [&](int t) { return q_full + 8 * (4 + t); };
-  auto o_done = [&](int t) { return q_full + 8 * (7 + t); };
+  auto s_full = [&](int t, int b) { return q_full + 8 * (1 + 2 * t + b); };
+  auto p_ready = [&](int t, int b) { return q_full + 8 * (5 + 2 * t + b); };
+  auto pv_done = [&](int t) { return q_full + 8 * (9 + t); };
+  auto o_done = [&](int t) { return q_full + 8 * (11 + t); };
+  const uint32_t s2_full = q_full + 8 * 14;
+  const uint32_t p2_ready = q_full + 8 * 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -262,11 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(empty_bar(i), ncons);  // one release per consumer of the chunk
     }
     ptx::mbar_init(q_full, kSoftmaxThreads);
-    for (int t = 0; t < 3; ++t) {
-      ptx::mbar_init(s_full(t), 1);
-      ptx::mbar_init(p_ready(t), 128);
-      ptx::mbar_init(o_done(t), 1);
+    for (int t = 0; t < 2; ++t) {
+      for (int b = 0; b < 2; ++b) {
+        ptx::mbar_init(s_full(t, b), 1);
+        ptx::mbar_init(p_ready(t, b), 128);
+      }
+      ptx::mbar_init(pv_done(t), 1);
     }
+    for (int t = 0; t < 3; ++t) ptx::mbar_init(o_done(t), 1);
+    ptx::mbar_init(s2_full, 1);
+    ptx::mbar_init(p2_ready, 128);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -315,81 +367,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kWarpMma) {
     // ------------------------------------------------------------ MMA issuers
     // One issuing thread per consumer: warp 13 main tile 0, warp 14 main tile 1,
-    // warp 15 the tail.  Each runs its consumer's chain in order: wait for the K/V
-    // stage, S = Q K^T, commit; wait for P, O += P V, release the stage.  Shared-
-    // memory descriptors are built once; a k-step only adds to the address field.
+    // warp 15 the tail.  Shared-memory descriptors are built once, split into a
+    // constant high word (stride, version, 128-byte swizzle) and a low word (start
+    // address >> 4, leading offset); a k-step only adds a constant to the low word.
     const int t = warp - kWarpMma;
     const bool mine = (t < 2) ? (t < n_main) : has_tail;
     if (lane == 0 && mine) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t idesc_qk_half = ptx::idesc_bf16_f32(128, 64, 0, 0);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t tS = tmem + (t == 0 ? C::kS0 : t == 1 ? C::kS1 : C::kS2);
-      const uint32_t tO = tmem + (t == 0 ? C::kO0 : t == 1 ? C::kO1 : C::kO2);
-      // Descriptors split into a constant high word (stride, version, 128-byte swizzle)
-      // and a low word (start address >> 4, leading offset); k-steps add constants.
-      const uint64_t dq = ptx::smem_desc_sw128(t == 0 ? sQ0 : t == 1 ? sQ1 : sQ2, 16, 1024);
-      const uint32_t hi = uint32_t(dq >> 32);
-      const uint32_t q_lo = uint32_t(dq);
+      const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sQ0, 16, 1024) >> 32);
       const uint32_t k0_lo = uint32_t(ptx::smem_desc_sw128(sK(0), 16, 1024));
       const uint32_t v0_lo = uint32_t(ptx::smem_desc_sw128(sV(0), kColBlockBytes, 1024));
-      constexpr uint32_t kStageStep = C::kStageBytes >> 4;  // 16-byte units
-      // S (+)= Q K^T over D: k-step k moves 32 bytes inside a 128-byte row, 16 KB per 64 columns
-      auto qk = [&](uint32_t k_lo, uint32_t idesc) {
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
-          if (k == 0) ptx::mma_ss_lh<0>(tS, q_lo + off, k_lo + off, hi, idesc);
-          else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc);
-        }
-      };
-      // O (+)= P V over KSTEPS x 16 keys: a k-step is 16 key rows (2 KB) of V and 8 TMEM columns of P
-      auto pv = [&](auto ksteps_tag, uint32_t v_lo, uint32_t p_col, uint32_t first_accumulate) {
-        constexpr int KSTEPS = decltype(ksteps_tag)::value;
-#pragma unroll
-        for (int k = 0; k < KSTEPS; ++k)
-          ptx::mma_ts_lh(tO, p_col + 8 * k, v_lo + uint32_t(128 * k), hi, idesc_pv, k == 0 ? first_accumulate : 1u);
-      };
-      using K8 = std::integral_constant<int, 8>;
-      using K4 = std::integral_constant<int, 4>;
+      constexpr uint32_t kStageStep = C::kStageBytes >> 4;       // 16-byte units
+      constexpr uint32_t kHalfRows = (kHalfKeys * 128) >> 4;     // 64 key rows of a K or V column block
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
-      const int nmma = dump ? (t < 2 ? min(n, 1) : 0) : n;
-      for (int c = 0; ok && c < nmma; ++c) {
-        const int st = c % S;
-        if (!(ok = ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag))) break;
-        ptx::tc_fence_after();
-        trace(p, kTrFullSeen, c);
-        const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
-        const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep;
-        const uint32_t acc0 = c > 0 ? 1u : 0u;
-        if (t < 2) {
-          qk(k_lo, idesc_qk);
-          ptx::mma_commit(s_full(t));
-          trace(p, t ? kTrQk1 : kTrQk0, c);
-          if (dump) break;
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(t), c & 1, limit, abort_flag))) break;
+      if (t < 2) {
+        constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kHalfKeys, 0, 0);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
+        const uint32_t q_lo = uint32_t(ptx::smem_desc_sw128(t ? sQ1 : sQ0, 16, 1024));
+        const uint32_t tO = tmem + (t ? C::kO1 : C::kO0);
+        const int halves = dump ? min(2 * n, 2) : 2 * n;
+        // S_t[g % 2] = Q_t K^T over the 64 keys of half chunk g
+        auto issue_qk = [&](int g) -> bool {
+          const int c = g >> 1, st = c % S;
+          if ((g & 1) == 0) {
+            if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
+            ptx::tc_fence_after();
+            if (t == 0) trace(p, kTrFullSeen, c);
+          }
+          const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep + uint32_t(g & 1) * kHalfRows;
+          const uint32_t tS = tmem + s_col(t, g & 1);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+            if (k == 0) ptx::mma_ss_lh<0>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
+            else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
+          }
+          ptx::mma_commit(s_full(t, g & 1));
+          trace(p, t ? kTrQk1 : ((g & 1) ? kTrQk0h1 : kTrQk0), c);
+          return true;
+        };
+        for (int g = 0; ok && g < min(halves, 2); ++g) ok = issue_qk(g);
+        for (int g = 0; ok && !dump && g < halves; ++g) {
+          const int b = g & 1, c = g >> 1, st = c % S;
+          if (!(ok = ptx::mbar_wait_bounded(p_ready(t, b), c & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
-          trace(p, t ? kTrP1Seen : kTrP0Seen, c);
-          pv(K8{}, v_lo, tS, acc0);
-        } else {
-          qk(k_lo, idesc_qk_half);                                  // keys 0..63
-          ptx::mma_commit(s_full(2));
-          trace(p, kTrQk2a, c);
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 0, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          trace(p, kTrP2aSeen, c);
-          pv(K4{}, v_lo, tS, acc0);
-          qk(k_lo + uint32_t(64 * 128 >> 4), idesc_qk_half);        // keys 64..127
-          ptx::mma_commit(s_full(2));
-          trace(p, kTrQk2b, c);
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(2), 1, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          trace(p, kTrP2bSeen, c);
-          pv(K4{}, v_lo + uint32_t(64 * 128 >> 4), tS, 1u);
+          trace(p, t ? kTrP1Seen : (b ? kTrP0h1Seen : kTrP0Seen), c);
+          // O_t (+)= P V over the half's 64 keys: a k-step is 16 key rows (2 KB) of V and
+          // 8 TMEM columns of packed P
+          const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep + uint32_t(b) * kHalfRows;
+          const uint32_t tP = tmem + s_col(t, b);
+#pragma unroll
+          for (int k = 0; k < kHalfKeys / 16; ++k)
+            ptx::mma_ts_lh(tO, tP + 8 * k, v_lo + uint32_t(128 * k), hi, idesc_pv, (g > 0 || k > 0) ? 1u : 0u);
+          ptx::mma_commit(pv_done(t));
+          if (b) {
+            ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
+            if (t == 0) trace(p, kTrEmpty, c);
+          }
+          if (g + 2 < halves) ok = issue_qk(g + 2);  // into the buffer the PV above reads (in order)
         }
-        ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
-        trace(p, kTrEmpty, c);
+      } else {
+        // Tail: S2^T = K Q2^T (M = 128 keys, N = 16 tail rows, K = 64), then
+        // O2 (+)= P2 V (M = 128, N = 64, K = 128 keys) with P2 from shared memory.
+        constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailMaxRows, 0, 0);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 64, 0, 1);
+        const uint32_t q2_lo = uint32_t(ptx::smem_desc_sw128(sQ2, 16, 1024));
+        const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
+        const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
+        const int nmma = dump ? 0 : n;
+        for (int c = 0; ok && c < nmma; ++c) {
+          const int st = c % S;
+          if (!(ok = ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (k == 0) ptx::mma_ss_lh<0>(tS2, k_lo, q2_lo, hi, idesc_st);
+            else ptx::mma_ss_lh<1>(tS2, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
+          }
+          ptx::mma_commit(s2_full);
+          trace(p, kTrQk2, c);
+          if (!(ok = ptx::mbar_wait_bounded(p2_ready, c & 1, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          trace(p, kTrP2Seen, c);
+          const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+            if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, p2_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
+            else ptx::mma_ss_lh<1>(tO2, p2_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
+          }
+          ptx::mma_commit(empty_bar(st));
+        }
       }
       if (!ok) signal_abort(p.status, abort_flag);
       ptx::mma_commit(o_done(t));  // arrives once every MMA this thread issued has completed
@@ -406,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = tile_on && row < p.T;
     const bool warp_on = tile_on && row0 + t * kTileRows + q4 * 32 < p.T;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    const uint32_t tS = tmem + (t ? C::kS1 : C::kS0) + lane_off;
+    const uint32_t tS0 = tmem + s_col(t, 0) + lane_off;  // buffer b at + 64 b
     const uint32_t tO = tmem + (t ? C::kO1 : C::kO0) + lane_off;
     const int64_t qrow = int64_t(work.stream) * p.T + row;
     if (tile_on)
@@ -417,61 +486,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_arrive(q_full);
 
     if (tile_on && dump) {
-      if (ptx::mbar_wait_warp(s_full(t), 0, limit, abort_flag) && n > 0) {
+      float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
+      for (int b = 0; b < 2 && n > 0; ++b) {
+        if (!ptx::mbar_wait_warp(s_full(t, b), 0, limit, abort_flag)) break;
         ptx::tc_fence_after();
-        float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           uint32_t s[32];
-          ptx::tmem_ld32(tS + 32 * j, s);
+          ptx::tmem_ld32(tS0 + kHalfKeys * b + 32 * j, s);
           ptx::tmem_wait_ld();
-          for (int e = 0; e < 32; ++e) dst[32 * j + e] = __uint_as_float(s[e]);
+          for (int e = 0; e < 32; ++e) dst[kHalfKeys * b + 32 * j + e] = __uint_as_float(s[e]);
         }
       }
     } else if (tile_on) {
       float m = -INFINITY;  // running max of scaled logits (log2 units)
       float l = 0.f;        // running sum of the bf16-rounded P
       bool ok = true;
+      int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
-      for (int j = 0; j < n; ++j) {
-        const int len = len_next;
-        if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
-        if (!(ok = ptx::mbar_wait_warp(s_full(t), j & 1, limit, abort_flag))) break;
+      for (int g = 0; g < 2 * n; ++g) {
+        const int b = g & 1;
+        if (b == 0) {
+          len = len_next;
+          if ((g >> 1) + 1 < n) len_next = __ldg(&p.chunks[c0 + (g >> 1) + 1].start_len) >> 16;
+        }
+        if (!(ok = ptx::mbar_wait_warp(s_full(t, b), (g >> 1) & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
-        if (q4 == 0 && lane == 0) trace(p, t ? kTrS1Seen : kTrS0Seen, j);
+        if (q4 == 0 && lane == 0) trace(p, t ? kTrS1Seen : (b ? kTrS0h1Seen : kTrS0Seen), g >> 1);
         if (warp_on) {
-          // One pass over S in 32-column quarters; the next quarter's TMEM load is in
-          // flight while this one is exponentiated.  The running max m only moves when
-          // a quarter's max exceeds it by more than 2^8; then O (earlier chunks), the
-          // P already written for this chunk and l are rescaled, so every P of the
-          // chunk shares one offset.  P of keys 32k..32k+31 goes to packed columns
-          // 16k..16k+15, which only overwrite S columns already read.
+          // One pass over the half's 64 scores in two 32-column quarters; the second
+          // quarter's TMEM load is in flight while the first is exponentiated.  The
+          // running max m only moves when a quarter's max exceeds it by more than 2^8.
+          // P of keys 32k..32k+31 goes to packed columns 16k..16k+15, which only
+          // overwrite S columns already read.  When m moved, O (every earlier half's
+          // PV, waited for) and the P of the first quarter are rescaled before P is
+          // handed to the MMA, so every P of the half shares one offset.
+          const uint32_t tS = tS0 + kHalfKeys * b;
           uint32_t qa[32], qb[32];
+          float corr_o = 1.f, corr_p = 1.f;
           ptx::tmem_ld32(tS, qa);
           ptx::tmem_wait_ld();
           auto quarter = [&](const int k, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
-            if (k < 3) ptx::tmem_ld32(tS + 32 * (k + 1), nxt);
-            mask32(cur, 32 * k, len);
+            if (k == 0) ptx::tmem_ld32(tS + 32, nxt);
+            mask32(cur, kHalfKeys * b + 32 * k, len);
             const float m_cand = max32(cur, -INFINITY) * sl2;
-            const bool need = m_cand > m + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-              const float m_new = need ? m_cand : m;
-              const float corr = need ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
-              rescale_running(tO, tS, j > 0 ? D : 0, 16 * k, corr);
+            if (m_cand > m + kRescaleThreshold) {
+              const float corr = ptx::ex2(m - m_cand);  // 0 while m is -inf
               l *= corr;
-              m = m_new;
+              corr_o *= corr;
+              if (k == 1) corr_p = corr;
+              m = m_cand;
             }
             l += exp_pack_store<32>(cur, sl2, -m, tS + 16 * k);
-            if (k < 3) ptx::tmem_wait_ld();
+            if (k == 0) ptx::tmem_wait_ld();
           };
           quarter(0, qa, qb);
           quarter(1, qb, qa);
-          quarter(2, qa, qb);
-          quarter(3, qb, qa);
           ptx::tmem_wait_st();
+          if (__any_sync(0xffffffffu, corr_o != 1.f) &&
+              !rescale_running(tO, tS, g > 0 ? D : 0, corr_o, corr_p, pv_done(t), uint32_t(g - 1) & 1u, limit,
+                               abort_flag)) {
+            ok = false;
+            break;
+          }
         }
         ptx::tc_fence_before();
-        if (q4 == 0 && lane == 0) trace(p, t ? kTrP1Arrive : kTrP0Arrive, j);
-        ptx::mbar_arrive(p_ready(t));
+        if (q4 == 0 && lane == 0) trace(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1);
+        ptx::mbar_arrive(p_ready(t, b));
       }
       if (!ok) signal_abort(p.status, abort_flag);
       if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
@@ -492,76 +572,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_arrive(q_full);
   } else {
     // ------------------------------------------------------------ tail softmax (warps 0-3)
-    const int q = warp;                       // lane quarter = key group
-    const int i = lane;                       // tail row
-    const bool row_ok = has_tail && i < p.tail_rows;
+    const int q = warp;  // TMEM lane quarter = key group [32q, 32q+32) of each chunk
+    const int tail_rows = p.tail_rows;
     const uint32_t lane_off = uint32_t(q * 32) << 16;
-    const uint32_t tS = tmem + C::kS2 + lane_off;
-    const uint32_t tO = tmem + C::kO2 + lane_off;
-    const int row = tail_row0 + i;
-    const int64_t qrow = int64_t(work.stream) * p.T + row;
-    if (has_tail)
-      store_q_row<D>(sQ2, q * 32 + i,
-                     reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D),
-                     row_ok);
+    const uint32_t tS2 = tmem + C::kS2 + lane_off;
+    const uint32_t tO2 = tmem + C::kO2 + lane_off;
+    if (has_tail) {
+      // zero the P tile (entries off the diagonal key-group blocks stay zero), then
+      // stage the tail's Q rows (rows past tail_rows are zero) as the MMA's B operand
+      const int idx = q * 32 + lane;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) st_shared_zero16(sP2 + uint32_t((i * 128 + idx) * 16));
+      const int qr = idx >> 3, qc = idx & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (qr < tail_rows) {
+        const int64_t qrow = int64_t(work.stream) * p.T + tail_row0 + qr;
+        v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D) +
+                  qc);
+      }
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ2 + uint32_t((qr >> 3) * 1024 + (qr & 7) * 128 +
+                                                                                 ((qc ^ (qr & 7)) << 4))),
+                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(q_full);
     if (has_tail && !dump) {
-      float m = -INFINITY, l = 0.f;
+      // per row r: m[r] warp-uniform running max (log2 units) of this key group,
+      // l[r] this lane's share of the row sum of the rounded P
+      float m[kTailMaxRows], l[kTailMaxRows];
+#pragma unroll
+      for (int rr = 0; rr < kTailMaxRows; ++rr) {
+        m[rr] = -INFINITY;
+        l[rr] = 0.f;
+      }
       bool ok = true;
+      const int key = 32 * q + lane;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
       for (int j = 0; ok && j < n; ++j) {
         const int len = len_next;
         if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
-        for (int h = 0; h < 2; ++h) {
-          if (!(ok = ptx::mbar_wait_warp(s_full(2), h, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          if (q == 0 && lane == 0) trace(p, h ? kTrS2bSeen : kTrS2aSeen, j);
-          const int key0 = 64 * h + 16 * q;
-          uint32_t s[16];
-          ptx::tmem_ld16(tS + 16 * q, s);
-          ptx::tmem_wait_ld();
-          float mx = -INFINITY;
+        if (!(ok = ptx::mbar_wait_warp(s2_full, j & 1, limit, abort_flag))) break;
+        ptx::tc_fence_after();
+        if (q == 0 && lane == 0) trace(p, kTrS2Seen, j);
+        uint32_t s[kTailMaxRows];
+        ptx::tmem_ld16(tS2, s);
+        ptx::tmem_wait_ld();
+        const bool valid = key < len;
+        bool resc = false;
+        float my_corr = 1.f;  // factor for the O2 row held by this lane (lane = tail row)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            if (key0 + e >= len) s[e] = __float_as_uint(-INFINITY);
-            mx = fmaxf(mx, __uint_as_float(s[e]));
+        for (int rr = 0; rr < kTailMaxRows; ++rr) {
+          if (rr < tail_rows) {
+            const float xs = valid ? __uint_as_float(s[rr]) * sl2 : -INFINITY;
+            const float mx = warp_max(xs);
+            if (mx > m[rr] + kRescaleThreshold) {  // warp-uniform
+              const float corr = ptx::ex2(m[rr] - mx);  // 0 while m is -inf
+              l[rr] *= corr;
+              if (lane == rr) my_corr = corr;
+              m[rr] = mx;
+              resc = true;
+            }
+            const float neg_m = (m[rr] == -INFINITY) ? 0.f : -m[rr];  // no key seen yet: p = 0
+            const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs + neg_m));
+            l[rr] += __bfloat162float(pb);
+            st_shared_u16(p2_addr(sP2, 32 * q + rr, key), __bfloat16_as_ushort(pb));
           }
-          const float m_cand = mx * sl2;
-          const bool need = m_cand > m + kRescaleThreshold;
-          const float m_new = need ? m_cand : m;
-          if ((j > 0 || h > 0) && __any_sync(0xffffffffu, need)) {
-            const float corr = need ? ptx::ex2(m - m_new) : 1.f;
-            rescale_tmem(tO, 64, corr);
-            l *= corr;
-          }
-          m = m_new;
-          const float neg_m = (m == -INFINITY) ? 0.f : -m;  // no key seen yet: every p is 0
-          uint32_t pk[8], zero[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pk[e] = pack_bf16(ptx::ex2(fmaf(__uint_as_float(s[2 * e]), sl2, neg_m)),
-                              ptx::ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, neg_m)));
-            l += packed_sum(pk[e]);
-            zero[e] = 0u;
-          }
-          // this lane quarter's P is nonzero only on its own 16 keys (packed columns 8q..8q+7)
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const uint32_t(&src)[8] = (b == q) ? pk : zero;
-            asm volatile(
-                "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(tS + 8 * b),
-                "r"(src[0]), "r"(src[1]), "r"(src[2]), "r"(src[3]), "r"(src[4]), "r"(src[5]), "r"(src[6]),
-                "r"(src[7])
-                : "memory");
-          }
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          if (q == 0 && lane == 0) trace(p, h ? kTrP2bArrive : kTrP2aArrive, j);
-          ptx::mbar_arrive(p_ready(2));
         }
+        if (resc && j > 0) {  // O2 holds the earlier chunks' PV (complete: it precedes this chunk's S2)
+          rescale_tmem(tO2, 64, my_corr);
+          ptx::tmem_wait_st();
+        }
+        ptx::fence_proxy_async_smem();  // P2 stores -> visible to the tensor core
+        ptx::tc_fence_before();
+        if (q == 0 && lane == 0) trace(p, kTrP2Arrive, j);
+        ptx::mbar_arrive(p2_ready);
       }
       if (!ok) signal_abort(p.status, abort_flag);
+      // this key group's (max, sum) of tail row `lane`
+      float my_m = -INFINITY, my_l = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < kTailMaxRows; ++rr) {
+        if (rr < tail_rows) {
+          const float lt = warp_sum(l[rr]);
+          if (lane == rr) {
+            my_m = m[rr];
+            my_l = lt;
+          }
+        }
+      }
       // merge the four key-group partial states of every tail row
       // The merge scratch reuses the K/V stage ring, so it may be written only once every
       // consumer's MMAs (and with them every load of this CTA) have completed.
@@ -573,34 +672,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u == 2 || u < n_main) done = ptx::mbar_wait_warp(o_done(u), 0, limit, abort_flag);
       if (done) {
         ptx::tc_fence_after();
+        if (lane < tail_rows) {
+          sm[q * kTailMaxRows + lane] = my_m;
+          sl[q * kTailMaxRows + lane] = my_l;
+        }
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
           uint32_t v[32];
-          ptx::tmem_ld32(tO + 32 * j, v);
+          ptx::tmem_ld32(tO2 + 32 * j, v);
           ptx::tmem_wait_ld();
-          if (row_ok) {
-            float4* dst = reinterpret_cast<float4*>(scratch + (q * kTailMaxRows + i) * 64 + 32 * j);
+          if (lane < tail_rows) {
+            float4* dst = reinterpret_cast<float4*>(scratch + (q * kTailMaxRows + lane) * 64 + 32 * j);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               dst[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
                                    __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
           }
         }
-        if (row_ok) {
-          sm[q * kTailMaxRows + i] = m;
-          sl[q * kTailMaxRows + i] = l;
-        }
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (done && !*abort_flag) {
-        for (int rr = q; rr < p.tail_rows; rr += 4) {
+        for (int rr = q; rr < tail_rows; rr += 4) {
           float mm = -INFINITY;
 #pragma unroll
           for (int g = 0; g < 4; ++g) mm = fmaxf(mm, sm[g * kTailMaxRows + rr]);
           float w[4], L = 0.f;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            w[g] = exp2f(sm[g * kTailMaxRows + rr] - mm);
+            // a key group that saw no valid key has m = -inf and contributes nothing
+            w[g] = sm[g * kTailMaxRows + rr] == -INFINITY ? 0.f : exp2f(sm[g * kTailMaxRows + rr] - mm);
             L += w[g] * sl[g * kTailMaxRows + rr];
           }
           float acc[2] = {0.f, 0.f};

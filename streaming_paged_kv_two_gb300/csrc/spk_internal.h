@@ -20,8 +20,8 @@ constexpr int kMaxSpecials = 64;
 constexpr int kTileRows = 128;
 // Events recorded by the bf16 attention kernel's trace mode (per chunk, CTA 0).
 enum TraceEvent {
-  kTrTmaIssue = 0, kTrFullSeen, kTrQk0, kTrP0Seen, kTrQk1, kTrP1Seen, kTrQk2a, kTrP2aSeen, kTrQk2b, kTrP2bSeen,
-  kTrEmpty, kTrS0Seen, kTrP0Arrive, kTrS1Seen, kTrP1Arrive, kTrS2aSeen, kTrP2aArrive, kTrS2bSeen, kTrP2bArrive,
+  kTrTmaIssue = 0, kTrFullSeen, kTrQk0, kTrP0Seen, kTrQk1, kTrP1Seen, kTrQk2, kTrP2Seen, kTrQk0h1, kTrP0h1Seen,
+  kTrEmpty, kTrS0Seen, kTrP0Arrive, kTrS1Seen, kTrP1Arrive, kTrS2Seen, kTrP2Arrive, kTrS0h1Seen, kTrP0h1Arrive,
   kTrLanded, kTraceEvents
 };
 // Device status word codes (first int32 of the workspace).
@@ -94,7 +94,7 @@ struct AttnParams {
   int32_t num_splits;
   int32_t ntiles;             // query tiles of kTileRows per stream (fp32 path)
   int32_t main_tiles;         // bf16 path: 128-row query tiles handled by full warpgroups
-  int32_t tail_rows;          // bf16 path: trailing rows (<= 32) handled by the key-split tail warps
+  int32_t tail_rows;          // bf16 path: trailing rows (<= 16) handled by the key-split tail warps
   int32_t ngroups;            // bf16 path: CTAs per (split, head): pairs of main tiles, the tail on the last
   float scale_log2;           // log2(e) / sqrt(D)
   long long wait_limit_ns;
