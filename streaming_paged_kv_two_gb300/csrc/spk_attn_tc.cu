@@ -38,7 +38,10 @@
 //               N=D, K=64) followed by Q K^T of half g+2 into the buffer just read.
 //               The consumers advance independently; a K/V stage is released once
 //               every consumer is done with it.
-// TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) | O0 | O1 [| O2 (64) | S2^T (16)].
+// TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) | O0 | O1, then for D = 64
+// O2 (64) | S2^T[0] | S2^T[1] (16 each).  With D = 64 the PV MMA's B operand is V
+// extended by a 16-column block of ones in shared memory, so O0/O1 are 80 columns wide
+// and column 64 accumulates the row sum of the bf16 P that the MMA consumed.
 // The epilogue writes bf16 output (one split) or an fp32 partial with its log2
 // log-sum-exp (several splits, combined by the merge kernel).
 // Every wait is bounded: on timeout the kernel records a status word, drains its
@@ -55,7 +58,8 @@ namespace {
 
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kTailMaxRows = 16;           // the N of the transposed tail MMA
+constexpr int kTailMaxRows = 8;            // rows of the tail (the transposed tail MMA has N = 16)
+constexpr int kTailN = 16;
 constexpr int kHalfKeys = 64;              // keys per main-tile score buffer
 constexpr int kThreads = 512;
 constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
@@ -67,23 +71,32 @@ template <int D>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;  // one Q, K or V tile in shared memory
   static constexpr bool kTail = (D == 64);
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // D == 64: the row sums come out of the PV MMA, whose B operand is V extended by a
+  // 16-column block of ones (O gets 16 more columns, each holding the row sum)
+  static constexpr bool kOnes = (D == 64);
+  static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kTile;
-  static constexpr int kQ2 = 2 * kTile;                 // tail Q: 16 rows x 128 bytes (D == 64)
-  static constexpr int kP2 = kQ2 + 2048;                // tail P: 128 rows x 128 keys bf16, two column blocks
-  static constexpr int kKV = kTail ? kP2 + 2 * kColBlockBytes : 2 * kTile;
+  static constexpr int kQ2 = 2 * kTile;                 // tail Q: kTailN rows x 128 bytes (D == 64)
+  static constexpr int kP2 = kQ2 + 2048;                // two tail P tiles: 128 rows x 128 keys bf16 each
+  static constexpr int kP2Bytes = 2 * kColBlockBytes;
+  static constexpr int kKV = kTail ? kP2 + 2 * kP2Bytes : 2 * kTile;
   static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kBars = kKV + kStages * kStageBytes;
-  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full, p2_ready
-  static constexpr int kNumBars = 2 * kStages + 16;
+  static constexpr int kOnesBlk = kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones (kOnes)
+  static constexpr int kBars = kOnesBlk + (kOnes ? kColBlockBytes : 0);
+  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full[2],
+  // p2_ready[2], pv2_done
+  static constexpr int kNumBars = 2 * kStages + 19;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + D;
-  static constexpr uint32_t kO2 = 4 * kHalfKeys + 2 * D, kS2 = kO2 + 64;  // D == 64 only
-  static_assert(kTail ? kS2 + kTailMaxRows <= 512 : kO1 + D <= 512, "TMEM budget");
-  static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
+  static constexpr int kOW = D + (kOnes ? 16 : 0);  // TMEM columns of a main tile's O
+  static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + kOW;
+  static constexpr uint32_t kO2 = 4 * kHalfKeys + 2 * kOW, kS2 = kO2 + 64;  // D == 64 only: O2, S2^T[2]
+  static_assert(kTail ? kS2 + 2 * kTailN <= 512 : kO1 + kOW <= 512, "TMEM budget");
+  static_assert(kTailN * 128 <= kP2 - kQ2, "tail Q tile");
+  static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kOnesBlk % 1024 == 0,
+                "128-byte-swizzled tiles start on 1024-byte boundaries");
   static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
   static_assert(kLaunch <= 227 * 1024, "shared memory per CTA");
 };
@@ -153,7 +166,7 @@ __device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src
 // p = 2^(s*sl2 - m) for N fp32 scores in registers, packed to bf16 pairs and stored to
 // TMEM at column `dst`; returns the fp32 sum of the rounded values.  The argument is
 // one packed fp32x2 FMA per pair and the sum adds the two bf16 halves directly.
-template <int N>
+template <int N, bool kSum>
 __device__ __forceinline__ float exp_pack_store(const uint32_t* s, float sl2, float neg_m, uint32_t dst) {
   static_assert(N % 32 == 0, "");
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
@@ -165,7 +178,7 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t* s, float sl2, fl
       float x0, x1;
       ptx::fma2(x0, x1, __uint_as_float(s[32 * j + 2 * e]), __uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m);
       pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
-      sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
+      if constexpr (kSum) sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
     }
     ptx::tmem_st16(dst + 16 * j, pk);
   }
@@ -191,15 +204,24 @@ __device__ __forceinline__ void mask32(uint32_t* s, int first_key, int len) {
   }
 }
 
-// Scale `ncols` TMEM columns of this warp's lanes by corr (per lane).
+// Scale `ncols` (a multiple of 16) TMEM columns of this warp's lanes by corr (per lane).
 __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float corr) {
-  for (int j = 0; j < ncols; j += 32) {
+  int j = 0;
+  for (; j + 32 <= ncols; j += 32) {
     uint32_t o[32];
     ptx::tmem_ld32(taddr + j, o);
     ptx::tmem_wait_ld();
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
     ptx::tmem_st32(taddr + j, o);
+  }
+  if (j < ncols) {
+    uint32_t o[16];
+    ptx::tmem_ld16(taddr + j, o);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+    ptx::tmem_st16(taddr + j, o);
   }
 }
 
@@ -278,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_ready = [&](int t, int b) { return q_full + 8 * (5 + 2 * t + b); };
   auto pv_done = [&](int t) { return q_full + 8 * (9 + t); };
   auto o_done = [&](int t) { return q_full + 8 * (11 + t); };
-  const uint32_t s2_full = q_full + 8 * 14;
-  const uint32_t p2_ready = q_full + 8 * 15;
+  auto s2_full = [&](int b) { return q_full + 8 * (14 + b); };
+  auto p2_ready = [&](int b) { return q_full + 8 * (16 + b); };
+  const uint32_t pv2_done = q_full + 8 * 18;
+  const uint32_t sOnes = sbase + C::kOnesBlk;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -317,8 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(pv_done(t), 1);
     }
     for (int t = 0; t < 3; ++t) ptx::mbar_init(o_done(t), 1);
-    ptx::mbar_init(s2_full, 1);
-    ptx::mbar_init(p2_ready, 128);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(s2_full(b), 1);
+      ptx::mbar_init(p2_ready(b), 128);
+    }
+    ptx::mbar_init(pv2_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
@@ -375,14 +402,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && mine) {
       const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sQ0, 16, 1024) >> 32);
       const uint32_t k0_lo = uint32_t(ptx::smem_desc_sw128(sK(0), 16, 1024));
-      const uint32_t v0_lo = uint32_t(ptx::smem_desc_sw128(sV(0), kColBlockBytes, 1024));
+      // V as an MN-major B operand: the leading offset is the distance to the next 64-column
+      // block (V's second half when D = 128, the ones block when the row sums ride along)
+      auto v_lo_of = [&](int st) {
+        return uint32_t(ptx::smem_desc_sw128(sV(st), C::kOnes ? sOnes - sV(st) : kColBlockBytes, 1024));
+      };
       constexpr uint32_t kStageStep = C::kStageBytes >> 4;       // 16-byte units
       constexpr uint32_t kHalfRows = (kHalfKeys * 128) >> 4;     // 64 key rows of a K or V column block
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
       if (t < 2) {
         constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kHalfKeys, 0, 0);
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, D, 0, 1);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, C::kOW, 0, 1);
         const uint32_t q_lo = uint32_t(ptx::smem_desc_sw128(t ? sQ1 : sQ0, 16, 1024));
         const uint32_t tO = tmem + (t ? C::kO1 : C::kO0);
         const int halves = dump ? min(2 * n, 2) : 2 * n;
@@ -414,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           trace(p, t ? kTrP1Seen : (b ? kTrP0h1Seen : kTrP0Seen), c);
           // O_t (+)= P V over the half's 64 keys: a k-step is 16 key rows (2 KB) of V and
           // 8 TMEM columns of packed P
-          const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep + uint32_t(b) * kHalfRows;
+          const uint32_t v_lo = v_lo_of(st) + uint32_t(b) * kHalfRows;
           const uint32_t tP = tmem + s_col(t, b);
 #pragma unroll
           for (int k = 0; k < kHalfKeys / 16; ++k)
@@ -429,35 +460,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // Tail: S2^T = K Q2^T (M = 128 keys, N = 16 tail rows, K = 64), then
         // O2 (+)= P2 V (M = 128, N = 64, K = 128 keys) with P2 from shared memory.
-        constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailMaxRows, 0, 0);
+        constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailN, 0, 0);
         constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 64, 0, 1);
         const uint32_t q2_lo = uint32_t(ptx::smem_desc_sw128(sQ2, 16, 1024));
         const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
         const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
         const int nmma = dump ? 0 : n;
-        for (int c = 0; ok && c < nmma; ++c) {
+        // S2^T[c % 2] = K_c Q2^T; issued two chunks ahead, right after the PV that read P2[c % 2]
+        auto issue_st = [&](int c) -> bool {
           const int st = c % S;
-          if (!(ok = ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag))) break;
+          if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
           ptx::tc_fence_after();
           const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
+          const uint32_t d = tS2 + uint32_t(kTailN * (c & 1));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            if (k == 0) ptx::mma_ss_lh<0>(tS2, k_lo, q2_lo, hi, idesc_st);
-            else ptx::mma_ss_lh<1>(tS2, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
+            if (k == 0) ptx::mma_ss_lh<0>(d, k_lo, q2_lo, hi, idesc_st);
+            else ptx::mma_ss_lh<1>(d, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
           }
-          ptx::mma_commit(s2_full);
+          ptx::mma_commit(s2_full(c & 1));
           trace(p, kTrQk2, c);
-          if (!(ok = ptx::mbar_wait_bounded(p2_ready, c & 1, limit, abort_flag))) break;
+          return true;
+        };
+        for (int c = 0; ok && c < min(nmma, 2); ++c) ok = issue_st(c);
+        for (int c = 0; ok && c < nmma; ++c) {
+          const int st = c % S;
+          if (!(ok = ptx::mbar_wait_bounded(p2_ready(c & 1), (c >> 1) & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace(p, kTrP2Seen, c);
-          const uint32_t v_lo = v0_lo + uint32_t(st) * kStageStep;
+          const uint32_t v_lo = v_lo_of(st);
+          const uint32_t a_lo = p2_lo + uint32_t((c & 1) * (C::kP2Bytes >> 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
-            if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, p2_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
-            else ptx::mma_ss_lh<1>(tO2, p2_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
+            if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
+            else ptx::mma_ss_lh<1>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
           }
+          ptx::mma_commit(pv2_done);
           ptx::mma_commit(empty_bar(st));
+          if (c + 2 < nmma) ok = issue_st(c + 2);
         }
       }
       if (!ok) signal_abort(p.status, abort_flag);
@@ -482,6 +523,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_q_row<D>(t ? sQ1 : sQ0, r,
                      reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D),
                      row_ok);
+    if constexpr (C::kOnes) {  // the ones block: 16 KB over the 256 main-softmax threads
+      const uint32_t ones = 0x3F803F80u;  // two bf16 1.0
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sOnes + uint32_t(((i * 256) + (threadIdx.x - 128)) * 16)),
+                     "r"(ones)
+                     : "memory");
+    }
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(q_full);
 
@@ -499,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (tile_on) {
       float m = -INFINITY;  // running max of scaled logits (log2 units)
-      float l = 0.f;        // running sum of the bf16-rounded P
+      float l = 0.f;        // running sum of the bf16-rounded P (without the ones block)
       bool ok = true;
       int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
@@ -531,19 +580,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_cand = max32(cur, -INFINITY) * sl2;
             if (m_cand > m + kRescaleThreshold) {
               const float corr = ptx::ex2(m - m_cand);  // 0 while m is -inf
-              l *= corr;
+              if constexpr (!C::kOnes) l *= corr;
               corr_o *= corr;
               if (k == 1) corr_p = corr;
               m = m_cand;
             }
-            l += exp_pack_store<32>(cur, sl2, -m, tS + 16 * k);
+            const float ps = exp_pack_store<32, !C::kOnes>(cur, sl2, -m, tS + 16 * k);
+            if constexpr (!C::kOnes) l += ps;
             if (k == 0) ptx::tmem_wait_ld();
           };
           quarter(0, qa, qb);
           quarter(1, qb, qa);
           ptx::tmem_wait_st();
           if (__any_sync(0xffffffffu, corr_o != 1.f) &&
-              !rescale_running(tO, tS, g > 0 ? D : 0, corr_o, corr_p, pv_done(t), uint32_t(g - 1) & 1u, limit,
+              !rescale_running(tO, tS, g > 0 ? C::kOW : 0, corr_o, corr_p, pv_done(t), uint32_t(g - 1) & 1u, limit,
                                abort_flag)) {
             ok = false;
             break;
@@ -556,6 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) signal_abort(p.status, abort_flag);
       if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
         ptx::tc_fence_after();
+        if constexpr (C::kOnes) {  // the row sum, as accumulated by the PV MMA
+          uint32_t lv[16];
+          ptx::tmem_ld16(tO + D, lv);
+          ptx::tmem_wait_ld();
+          l = __uint_as_float(lv[0]);
+        }
         const float inv_l = 1.f / l;
 #pragma unroll 1
         for (int j = 0; j < D / 32; ++j) {
@@ -578,11 +634,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS2 = tmem + C::kS2 + lane_off;
     const uint32_t tO2 = tmem + C::kO2 + lane_off;
     if (has_tail) {
-      // zero the P tile (entries off the diagonal key-group blocks stay zero), then
+      // zero both P tiles (entries off the diagonal key-group blocks stay zero), then
       // stage the tail's Q rows (rows past tail_rows are zero) as the MMA's B operand
       const int idx = q * 32 + lane;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) st_shared_zero16(sP2 + uint32_t((i * 128 + idx) * 16));
+      for (int i = 0; i < 2 * C::kP2Bytes / (128 * 16); ++i) st_shared_zero16(sP2 + uint32_t((i * 128 + idx) * 16));
       const int qr = idx >> 3, qc = idx & 7;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (qr < tail_rows) {
@@ -612,41 +668,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int len = len_next;
         if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
-        if (!(ok = ptx::mbar_wait_warp(s2_full, j & 1, limit, abort_flag))) break;
+        if (!(ok = ptx::mbar_wait_warp(s2_full(j & 1), (j >> 1) & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
         if (q == 0 && lane == 0) trace(p, kTrS2Seen, j);
-        uint32_t s[kTailMaxRows];
-        ptx::tmem_ld16(tS2, s);
+        uint32_t s[16];
+        ptx::tmem_ld16(tS2 + uint32_t(kTailN * (j & 1)), s);
         ptx::tmem_wait_ld();
+        // The row offsets m[r] are only refreshed (an exact warp max) when some lane's
+        // score exceeds them by more than 2^8, so the common chunk needs no reduction.
         const bool valid = key < len;
-        bool resc = false;
-        float my_corr = 1.f;  // factor for the O2 row held by this lane (lane = tail row)
+        float xs[kTailMaxRows];
+        uint32_t need = 0;
 #pragma unroll
         for (int rr = 0; rr < kTailMaxRows; ++rr) {
-          if (rr < tail_rows) {
-            const float xs = valid ? __uint_as_float(s[rr]) * sl2 : -INFINITY;
-            const float mx = warp_max(xs);
-            if (mx > m[rr] + kRescaleThreshold) {  // warp-uniform
+          xs[rr] = valid ? __uint_as_float(s[rr]) * sl2 : -INFINITY;
+          if (rr < tail_rows && xs[rr] > m[rr] + kRescaleThreshold) need |= 1u << rr;
+        }
+        const uint32_t rows_moved = __reduce_or_sync(0xffffffffu, need);
+        if (rows_moved) {
+          float my_corr = 1.f;  // factor for the O2 row held by this lane (lane = tail row)
+#pragma unroll
+          for (int rr = 0; rr < kTailMaxRows; ++rr) {
+            if ((rows_moved >> rr) & 1u) {
+              const float mx = warp_max(xs[rr]);
               const float corr = ptx::ex2(m[rr] - mx);  // 0 while m is -inf
               l[rr] *= corr;
               if (lane == rr) my_corr = corr;
               m[rr] = mx;
-              resc = true;
             }
-            const float neg_m = (m[rr] == -INFINITY) ? 0.f : -m[rr];  // no key seen yet: p = 0
-            const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs + neg_m));
-            l[rr] += __bfloat162float(pb);
-            st_shared_u16(p2_addr(sP2, 32 * q + rr, key), __bfloat16_as_ushort(pb));
+          }
+          if (j > 0) {  // O2 must first hold the previous chunk's PV
+            if (!ptx::mbar_wait_warp(pv2_done, uint32_t(j - 1) & 1u, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            rescale_tmem(tO2, 64, my_corr);
+            ptx::tmem_wait_st();
           }
         }
-        if (resc && j > 0) {  // O2 holds the earlier chunks' PV (complete: it precedes this chunk's S2)
-          rescale_tmem(tO2, 64, my_corr);
-          ptx::tmem_wait_st();
+#pragma unroll
+        for (int rr = 0; rr < kTailMaxRows; ++rr) {
+          if (rr < tail_rows) {
+            const float neg_m = (m[rr] == -INFINITY) ? 0.f : -m[rr];  // no key seen yet: p = 0
+            const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs[rr] + neg_m));
+            l[rr] += __bfloat162float(pb);
+            st_shared_u16(p2_addr(sP2 + uint32_t((j & 1) * C::kP2Bytes), 32 * q + rr, key), __bfloat16_as_ushort(pb));
+          }
         }
         ptx::fence_proxy_async_smem();  // P2 stores -> visible to the tensor core
         ptx::tc_fence_before();
         if (q == 0 && lane == 0) trace(p, kTrP2Arrive, j);
-        ptx::mbar_arrive(p2_ready);
+        ptx::mbar_arrive(p2_ready(j & 1));
       }
       if (!ok) signal_abort(p.status, abort_flag);
       // this key group's (max, sum) of tail row `lane`

@@ -208,7 +208,8 @@ CASES = {
     "f32_d128_streams": (small(dtype="f32", head_dim=128, num_streams=2, frames=5, value_scale=1.0), 3),
     "per_head_scale_d128": (small(head_dim=128, per_head_scale=True, num_streams=2, frames=5, shuffle_pages=True), 0),
     "t1_row": (small(patches_per_frame=1, specials_per_frame=1, page_size=16, frames=12), 0),
-    "t144_tail16": (small(patches_per_frame=138, page_size=256, frames=6), 2),
+    "t136_tail8": (small(patches_per_frame=130, page_size=256, frames=6), 2),
+    "t144_rem16_main": (small(patches_per_frame=138, page_size=256, frames=6), 2),
     "t150_rem22_main": (small(patches_per_frame=144, page_size=256, frames=6), 0),
     "t6_tail_only": (small(patches_per_frame=3, specials_per_frame=3, page_size=16, frames=10), 2),
 }
