@@ -163,24 +163,21 @@ __device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src
   }
 }
 
-// p = 2^(s*sl2 - m) for N fp32 scores in registers, packed to bf16 pairs and stored to
-// TMEM at column `dst`; returns the fp32 sum of the rounded values.  The argument is
-// one packed fp32x2 FMA per pair and the sum adds the two bf16 halves directly.
-template <int N, bool kSum>
-__device__ __forceinline__ float exp_pack_store(const uint32_t* s, float sl2, float neg_m, uint32_t dst) {
-  static_assert(N % 32 == 0, "");
+// p = 2^(s*sl2 - m) for the 64 fp32 scores of a half chunk (two 32-column quarters),
+// packed to bf16 pairs in pk; returns the fp32 sum of the rounded values when kSum.  The
+// argument is one packed fp32x2 FMA per pair and the sum adds the two bf16 halves directly.
+template <bool kSum>
+__device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* sb, float sl2, float neg_m,
+                                            uint32_t (&pk)[32]) {
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < N / 32; ++j) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float x0, x1;
-      ptx::fma2(x0, x1, __uint_as_float(s[32 * j + 2 * e]), __uint_as_float(s[32 * j + 2 * e + 1]), sl2, neg_m);
-      pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
-      if constexpr (kSum) sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
-    }
-    ptx::tmem_st16(dst + 16 * j, pk);
+  for (int e = 0; e < 32; ++e) {
+    const uint32_t* s = e < 16 ? sa : sb;
+    const int i = 2 * (e & 15);
+    float x0, x1;
+    ptx::fma2(x0, x1, __uint_as_float(s[i]), __uint_as_float(s[i + 1]), sl2, neg_m);
+    pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
+    if constexpr (kSum) sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
   }
   return (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
@@ -225,36 +222,33 @@ __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float co
   }
 }
 
-// Scale the bf16 pairs in packed TMEM columns [0, ncols) of this warp's lanes by corr.
-__device__ __forceinline__ void rescale_packed_p(uint32_t taddr, int ncols, float corr) {
-  for (int j = 0; j < ncols; j += 16) {
-    uint32_t v[16];
-    ptx::tmem_ld16(taddr + j, v);
-    ptx::tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-      v[e] = pack_bf16(__uint_as_float(v[e] << 16) * corr, __uint_as_float(v[e] & 0xFFFF0000u) * corr);
-    ptx::tmem_st16(taddr + j, v);
-  }
-}
-
 // Rare path of the online softmax (kept out of line so the hot loop's registers are
-// not spent on it), taken at the end of a half chunk in which some row's running max
-// moved: wait until O holds every earlier PV (when o_cols > 0: the PV of the previous
-// half, tracked by pv_bar), scale the first o_cols columns of O by corr_o and the
-// half's first quarter of packed P (16 columns) by corr_p.  False when the wait gave up.
-__device__ __noinline__ bool rescale_running(uint32_t tO, uint32_t tS, int o_cols, float corr_o, float corr_p,
-                                             uint32_t pv_bar, uint32_t parity, long long limit,
-                                             const volatile int* abort_flag) {
+// not spent on it), taken when some row of the warp saw a score above its running max
+// m by more than 2^8: the row moves to m_new; O (every earlier PV of this tile: when
+// o_cols > 0, wait for the previous half's PV, tracked by pv_bar) is scaled by
+// corr = 2^(m - m_new), and the half's P is recomputed from S (still in TMEM) with
+// the new offset and stored over it.  Returns the sum of the new rounded P (when
+// kSum) and whether the wait succeeded.
+template <bool kSum>
+__device__ __noinline__ float2 move_running_max(uint32_t tO, uint32_t tS, int o_cols, float corr, float neg_m,
+                                                float sl2, int first_key, int len, uint32_t pv_bar, uint32_t parity,
+                                                long long limit, const volatile int* abort_flag) {
   bool ok = true;
   if (o_cols) {
     ok = ptx::mbar_wait_warp(pv_bar, parity, limit, abort_flag);
     ptx::tc_fence_after();
-    rescale_tmem(tO, o_cols, corr_o);
+    rescale_tmem(tO, o_cols, corr);
   }
-  rescale_packed_p(tS, 16, corr_p);
+  uint32_t sa[32], sb[32], pk[32];
+  ptx::tmem_ld32(tS, sa);
+  ptx::tmem_ld32(tS + 32, sb);
+  ptx::tmem_wait_ld();
+  mask32(sa, first_key, len);
+  mask32(sb, first_key + 32, len);
+  const float sum = exp_pack64<kSum>(sa, sb, sl2, neg_m, pk);
+  ptx::tmem_st32(tS, pk);
   ptx::tmem_wait_st();
-  return ok;
+  return make_float2(sum, ok ? 1.f : 0.f);
 }
 
 // Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
@@ -466,7 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
         const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
         const int nmma = dump ? 0 : n;
-        // S2^T[c % 2] = K_c Q2^T; issued two chunks ahead, right after the PV that read P2[c % 2]
+        // S2^T[c % 2] = K_c Q2^T, issued one chunk ahead: before waiting for P2 of chunk c-1
+        // (its buffer was read by the softmax of chunk c-2, whose PV precedes it)
         auto issue_st = [&](int c) -> bool {
           const int st = c % S;
           if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
@@ -482,9 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           trace(p, kTrQk2, c);
           return true;
         };
-        for (int c = 0; ok && c < min(nmma, 2); ++c) ok = issue_st(c);
+        if (nmma > 0) ok = issue_st(0);
         for (int c = 0; ok && c < nmma; ++c) {
           const int st = c % S;
+          if (c + 1 < nmma && !(ok = issue_st(c + 1))) break;
           if (!(ok = ptx::mbar_wait_bounded(p2_ready(c & 1), (c >> 1) & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace(p, kTrP2Seen, c);
@@ -498,7 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mma_commit(pv2_done);
           ptx::mma_commit(empty_bar(st));
-          if (c + 2 < nmma) ok = issue_st(c + 2);
         }
       }
       if (!ok) signal_abort(p.status, abort_flag);
@@ -562,41 +557,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         if (q4 == 0 && lane == 0) trace(p, t ? kTrS1Seen : (b ? kTrS0h1Seen : kTrS0Seen), g >> 1);
         if (warp_on) {
-          // One pass over the half's 64 scores in two 32-column quarters; the second
-          // quarter's TMEM load is in flight while the first is exponentiated.  The
-          // running max m only moves when a quarter's max exceeds it by more than 2^8.
-          // P of keys 32k..32k+31 goes to packed columns 16k..16k+15, which only
-          // overwrite S columns already read.  When m moved, O (every earlier half's
-          // PV, waited for) and the P of the first quarter are rescaled before P is
-          // handed to the MMA, so every P of the half shares one offset.
+          // The half's 64 scores are exponentiated against the running max m while
+          // their own max is taken; only when a score exceeds m by more than 2^8 (in
+          // practice: the first half, and rare jumps) does the warp take the out-of-line
+          // path that moves m, rescales O and recomputes this half's P.  P (packed
+          // bf16 pairs) overwrites the first 32 columns of the half's S buffer.
           const uint32_t tS = tS0 + kHalfKeys * b;
-          uint32_t qa[32], qb[32];
-          float corr_o = 1.f, corr_p = 1.f;
-          ptx::tmem_ld32(tS, qa);
+          uint32_t sa[32], sb[32], pk[32];
+          ptx::tmem_ld32(tS, sa);
+          ptx::tmem_ld32(tS + 32, sb);
           ptx::tmem_wait_ld();
-          auto quarter = [&](const int k, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
-            if (k == 0) ptx::tmem_ld32(tS + 32, nxt);
-            mask32(cur, kHalfKeys * b + 32 * k, len);
-            const float m_cand = max32(cur, -INFINITY) * sl2;
-            if (m_cand > m + kRescaleThreshold) {
-              const float corr = ptx::ex2(m - m_cand);  // 0 while m is -inf
-              if constexpr (!C::kOnes) l *= corr;
-              corr_o *= corr;
-              if (k == 1) corr_p = corr;
-              m = m_cand;
+          mask32(sa, kHalfKeys * b, len);
+          mask32(sb, kHalfKeys * b + 32, len);
+          const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
+          const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk);
+          const bool need = mx > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = need ? mx : m;
+            const float corr = need ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
+            const float2 r2 = move_running_max<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, corr, -m_new, sl2,
+                                                           kHalfKeys * b, len, pv_done(t), uint32_t(g - 1) & 1u,
+                                                           limit, abort_flag);
+            if constexpr (!C::kOnes) l = l * corr + r2.x;
+            m = m_new;
+            if (r2.y == 0.f) {
+              ok = false;
+              break;
             }
-            const float ps = exp_pack_store<32, !C::kOnes>(cur, sl2, -m, tS + 16 * k);
+          } else {
+            ptx::tmem_st32(tS, pk);
             if constexpr (!C::kOnes) l += ps;
-            if (k == 0) ptx::tmem_wait_ld();
-          };
-          quarter(0, qa, qb);
-          quarter(1, qb, qa);
-          ptx::tmem_wait_st();
-          if (__any_sync(0xffffffffu, corr_o != 1.f) &&
-              !rescale_running(tO, tS, g > 0 ? C::kOW : 0, corr_o, corr_p, pv_done(t), uint32_t(g - 1) & 1u, limit,
-                               abort_flag)) {
-            ok = false;
-            break;
+            ptx::tmem_wait_st();
           }
         }
         ptx::tc_fence_before();
