@@ -266,12 +266,12 @@ __device__ __forceinline__ void store_output_cols(const AttnParams& p, const Wor
                           pack_bf16(__uint_as_float(v[8 * k + 4]) * scale, __uint_as_float(v[8 * k + 5]) * scale),
                           pack_bf16(__uint_as_float(v[8 * k + 6]) * scale, __uint_as_float(v[8 * k + 7]) * scale));
   } else {
-    const int64_t idx = (int64_t(split) * p.H + head) * p.T + row;
-    float4* dst = reinterpret_cast<float4*>(p.part_o + idx * D + col0);
+    // one float4 per column group; the 32 rows of a warp write 512 contiguous bytes
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-      dst[k] = make_float4(__uint_as_float(v[4 * k]) * scale, __uint_as_float(v[4 * k + 1]) * scale,
-                           __uint_as_float(v[4 * k + 2]) * scale, __uint_as_float(v[4 * k + 3]) * scale);
+      *reinterpret_cast<float4*>(p.part_o + part_o_offset<D>(split, head, row, col0 + 4 * k, p.H, p.T)) =
+          make_float4(__uint_as_float(v[4 * k]) * scale, __uint_as_float(v[4 * k + 1]) * scale,
+                      __uint_as_float(v[4 * k + 2]) * scale, __uint_as_float(v[4 * k + 3]) * scale);
   }
 }
 
@@ -547,7 +547,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
-      for (int g = 0; g < 2 * n; ++g) {
+      if (warp_on && n > 0) {
+        // the first half sets the running max from its own scores (nothing to rescale yet)
+        if ((ok = ptx::mbar_wait_warp(s_full(t, 0), 0, limit, abort_flag))) {
+          ptx::tc_fence_after();
+          uint32_t sa[32], sb[32];
+          ptx::tmem_ld32(tS0, sa);
+          ptx::tmem_ld32(tS0 + 32, sb);
+          ptx::tmem_wait_ld();
+          mask32(sa, 0, len_next);
+          mask32(sb, 32, len_next);
+          m = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
+        }
+      }
+      for (int g = 0; ok && g < 2 * n; ++g) {
         const int b = g & 1;
         if (b == 0) {
           len = len_next;
@@ -782,7 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[lane] = pack_bf16(acc[0] * inv, acc[1] * inv);
           } else {
             const int64_t idx = (int64_t(split) * p.H + head) * p.T + orow;
-            reinterpret_cast<float2*>(p.part_o + idx * D)[lane] = make_float2(acc[0] * inv, acc[1] * inv);
+            *reinterpret_cast<float2*>(p.part_o + part_o_offset<D>(split, head, orow, 2 * lane, p.H, p.T)) =
+                make_float2(acc[0] * inv, acc[1] * inv);
             if (lane == 0) p.part_lse[idx] = mm + __log2f(L);
           }
         }

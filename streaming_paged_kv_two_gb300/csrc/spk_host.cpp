@@ -531,32 +531,20 @@ int spk_plan(spk_cache* c, void* workspace, void* cuda_stream) {
 
 namespace {
 
-int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* workspace, void* cuda_stream,
-                       float* dump_scores, unsigned long long* trace = nullptr, int32_t trace_cap = 0) {
-  int rc = check_cache(c);
-  if (rc) return rc;
+// Parameters of block's attention launch over the current plan, with the split-KV
+// partials at part_o / part_lse.
+AttnParams attention_params(const spk_cache* c, int block, const void* q, void* out, char* ws, float* part_o,
+                            float* part_lse) {
   const spk_config& g = c->cfg;
-  if (c->dry) return fail(SPK_ERR_INVALID_ARG, "bookkeeping-only cache cannot run attention");
-  if (block < 0 || block >= g.num_blocks) return fail(SPK_ERR_INVALID_ARG, "block %d out of range", block);
-  if (!q || !workspace || (!out && !dump_scores)) return fail(SPK_ERR_INVALID_ARG, "q, out and workspace must be device pointers");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
-    return fail(SPK_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
-  if (dump_scores && g.dtype != SPK_BF16) return fail(SPK_ERR_INVALID_ARG, "score dump exists for the bf16 kernel only");
-  if (!c->plan_valid) return fail(SPK_ERR_BAD_STATE, "no current plan: call spk_plan after append/evict");
-  if (workspace != c->plan_ws) return fail(SPK_ERR_INVALID_ARG, "workspace differs from the one given to spk_plan");
-  for (int s = 0; s < g.num_streams; ++s)
-    if (!c->st[s].appended[block])
-      return fail(SPK_ERR_BAD_STATE, "block %d of stream %d not appended in the current frame", block, s);
   const WorkspaceLayout& L = c->ws;
-  char* ws = static_cast<char*>(workspace);
   AttnParams p{};
   p.pool = c->pools[block];
   p.q = q;
   p.out = out;
   p.chunks = reinterpret_cast<const ChunkDesc*>(ws + L.chunks);
   p.works = reinterpret_cast<const WorkDesc*>(ws + L.works);
-  p.part_o = reinterpret_cast<float*>(ws + L.part_o);
-  p.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  p.part_o = part_o;
+  p.part_lse = part_lse;
   p.status = reinterpret_cast<int32_t*>(ws + L.status);
   p.row_stride = int64_t(g.num_heads) * g.head_dim;
   p.half_stride = int64_t(g.page_size) * p.row_stride;
@@ -575,19 +563,22 @@ int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* 
   }
   p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(g.head_dim)));
   p.wait_limit_ns = c->wait_limit_ns;
-  p.dump_scores = dump_scores;
-  p.trace = trace;
-  p.trace_cap = trace_cap;
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  return p;
+}
+
+// Launch the attention kernel, then, when a stream has several KV splits, the merge
+// of their partials (not in score-dump mode, which writes no output).
+int launch_attention(const spk_cache* c, int block, const AttnParams& p, char* ws, cudaStream_t stream) {
+  const spk_config& g = c->cfg;
   cudaError_t e = g.dtype == SPK_BF16 ? launch_attention_bf16(p, &c->maps[block], stream)
                                       : launch_attention_f32(p, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-  if (c->info.merge_needed && !dump_scores) {
+  if (c->info.merge_needed && !p.dump_scores) {
     MergeParams m{};
     m.part_o = p.part_o;
     m.part_lse = p.part_lse;
-    m.streams = reinterpret_cast<const StreamDesc*>(ws + L.streams);
-    m.out = out;
+    m.streams = reinterpret_cast<const StreamDesc*>(ws + c->ws.streams);
+    m.out = p.out;
     m.B = g.num_streams;
     m.T = c->T;
     m.H = g.num_heads;
@@ -596,6 +587,32 @@ int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* 
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
   }
   return SPK_OK;
+}
+
+int run_attention_impl(spk_cache* c, int block, const void* q, void* out, void* workspace, void* cuda_stream,
+                       float* dump_scores, unsigned long long* trace = nullptr, int32_t trace_cap = 0) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  const spk_config& g = c->cfg;
+  if (c->dry) return fail(SPK_ERR_INVALID_ARG, "bookkeeping-only cache cannot run attention");
+  if (block < 0 || block >= g.num_blocks) return fail(SPK_ERR_INVALID_ARG, "block %d out of range", block);
+  if (!q || !workspace || (!out && !dump_scores)) return fail(SPK_ERR_INVALID_ARG, "q, out and workspace must be device pointers");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(SPK_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (dump_scores && g.dtype != SPK_BF16) return fail(SPK_ERR_INVALID_ARG, "score dump exists for the bf16 kernel only");
+  if (!c->plan_valid) return fail(SPK_ERR_BAD_STATE, "no current plan: call spk_plan after append/evict");
+  if (workspace != c->plan_ws) return fail(SPK_ERR_INVALID_ARG, "workspace differs from the one given to spk_plan");
+  for (int s = 0; s < g.num_streams; ++s)
+    if (!c->st[s].appended[block])
+      return fail(SPK_ERR_BAD_STATE, "block %d of stream %d not appended in the current frame", block, s);
+  const WorkspaceLayout& L = c->ws;
+  char* ws = static_cast<char*>(workspace);
+  AttnParams p = attention_params(c, block, q, out, ws, reinterpret_cast<float*>(ws + L.part_o),
+                                  reinterpret_cast<float*>(ws + L.part_lse));
+  p.dump_scores = dump_scores;
+  p.trace = trace;
+  p.trace_cap = trace_cap;
+  return launch_attention(c, block, p, ws, static_cast<cudaStream_t>(cuda_stream));
 }
 
 }  // namespace
@@ -646,50 +663,11 @@ int spk_run_attention_static_scratch(spk_cache* c, int block, const void* q, voi
   void* scratch = nullptr;
   cudaError_t e = static_scratch_address(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
-  const WorkspaceLayout& L = c->ws;
   char* ws = static_cast<char*>(workspace);
-  AttnParams p{};
-  p.pool = c->pools[block];
-  p.q = q;
-  p.out = out;
-  p.chunks = reinterpret_cast<const ChunkDesc*>(ws + L.chunks);
-  p.works = reinterpret_cast<const WorkDesc*>(ws + L.works);
-  p.part_o = static_cast<float*>(scratch);
-  p.part_lse = reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes);
-  p.status = reinterpret_cast<int32_t*>(ws + L.status);
-  p.row_stride = int64_t(g.num_heads) * g.head_dim;
-  p.half_stride = int64_t(g.page_size) * p.row_stride;
-  p.page_stride = 2 * p.half_stride;
-  p.T = c->T;
-  p.H = g.num_heads;
-  p.D = g.head_dim;
-  p.ps = g.page_size;
-  p.num_splits = c->info.num_splits;
-  p.ntiles = (c->T + kTileRows - 1) / kTileRows;
-  {
-    const TileShape ts = attention_bf16_tiles(c->T, g.head_dim);
-    p.main_tiles = ts.main_tiles;
-    p.tail_rows = ts.tail_rows;
-    p.ngroups = ts.ngroups;
-  }
-  p.scale_log2 = float(1.4426950408889634 / std::sqrt(double(g.head_dim)));
-  p.wait_limit_ns = c->wait_limit_ns;
-  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  e = g.dtype == SPK_BF16 ? launch_attention_bf16(p, &c->maps[block], stream) : launch_attention_f32(p, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-  if (c->info.merge_needed) {
-    MergeParams m{};
-    m.part_o = p.part_o;
-    m.part_lse = p.part_lse;
-    m.streams = reinterpret_cast<const StreamDesc*>(ws + L.streams);
-    m.out = out;
-    m.B = g.num_streams;
-    m.T = c->T;
-    m.H = g.num_heads;
-    m.D = g.head_dim;
-    e = launch_merge(m, g.dtype, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-  }
+  const AttnParams p = attention_params(c, block, q, out, ws, static_cast<float*>(scratch),
+                                        reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes));
+  rc = launch_attention(c, block, p, ws, static_cast<cudaStream_t>(cuda_stream));
+  if (rc) return rc;
   return ok();
 }
 

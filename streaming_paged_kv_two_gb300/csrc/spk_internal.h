@@ -58,7 +58,7 @@ struct WorkspaceLayout {
   size_t chunks = 0;     // ChunkDesc[max_chunks]
   size_t works = 0;      // WorkDesc[max_splits]
   size_t plan_end = 0;   // end of the part uploaded by plan
-  size_t part_o = 0;     // float[max_splits][H][T][D]
+  size_t part_o = 0;     // float[max_splits][H][D/4][T][4] (see part_o_offset)
   size_t part_lse = 0;   // float[max_splits][H][T]  (log2 units)
   size_t total = 0;
   int64_t max_chunks = 0;
@@ -103,6 +103,15 @@ struct AttnParams {
   float* dump_scores;         // diagnostics only: non-NULL makes the bf16 kernel write the raw
                               // Q K^T tile of each CTA's first chunk ([ctas][128][128] fp32) and stop
 };
+
+// Offset (in floats) of element d of query row `row` in the split-KV partial O of
+// (split, head): the layout is [split][head][d/4][row][4], so the float4s of 32
+// consecutive rows at one column group are contiguous (the attention kernels store
+// one row per thread; the merge reads one row per thread).
+template <int D>
+__host__ __device__ inline int64_t part_o_offset(int split, int head, int row, int d, int H, int T) {
+  return (((int64_t(split) * H + head) * (D / 4) + d / 4) * T + row) * 4 + (d & 3);
+}
 
 struct MergeParams {
   const float* part_o;

@@ -49,33 +49,35 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
 // ------------------------------------------------------------------ merge
 // Exact recombination of softmax attention over disjoint key sets: with
 // M = max_j lse_j (log2 units) and w_j = 2^(lse_j - M),
-// out = sum_j w_j O_j / sum_j w_j.  One thread per (query row, head, 4 columns); the
-// split loop is unrolled so the partial loads of several splits are in flight.
+// out = sum_j w_j O_j / sum_j w_j.  One thread per (stream, head, 4 columns, query
+// row), rows fastest, so a warp reads 32 consecutive rows' float4s of a split in one
+// 512-byte run; the split loop is unrolled so the loads of several splits are in flight.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   constexpr int V = D / 4;  // float4 per row
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = int64_t(p.B) * p.T * p.H * V;
+  const int64_t total = int64_t(p.B) * p.H * V * p.T;
   if (idx >= total) return;
-  const int c4 = int(idx % V);
-  const int64_t rh = idx / V;
-  const int h = int(rh % p.H);
-  const int row = int(rh / p.H);
-  const int s = row / p.T;
-  const int t = row - s * p.T;
+  const int t = int(idx % p.T);
+  int64_t rest = idx / p.T;
+  const int c4 = int(rest % V);
+  rest /= V;
+  const int h = int(rest % p.H);
+  const int s = int(rest / p.H);
   const StreamDesc sd = p.streams[s];
   if (sd.nsplit <= 1) return;  // written by the attention kernel
-  const int64_t base = (int64_t(sd.split_base) * p.H + h) * p.T + t;  // partial index of split 0
-  const int64_t step = int64_t(p.H) * p.T;                            // next split, same (head, row)
+  const int64_t lse0 = (int64_t(sd.split_base) * p.H + h) * p.T + t;  // split 0's log-sum-exp
+  const int64_t lse_step = int64_t(p.H) * p.T;                         // next split, same (head, row)
+  const int64_t o0 = part_o_offset<D>(sd.split_base, h, t, 4 * c4, p.H, p.T);
+  const int64_t o_step = int64_t(p.H) * D * p.T;
   float m = -INFINITY;
-  for (int j = 0; j < sd.nsplit; ++j) m = fmaxf(m, __ldg(&p.part_lse[base + j * step]));
+  for (int j = 0; j < sd.nsplit; ++j) m = fmaxf(m, __ldg(&p.part_lse[lse0 + j * lse_step]));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
 #pragma unroll 4
   for (int j = 0; j < sd.nsplit; ++j) {
-    const int64_t pi = base + j * step;
-    const float w = exp2f(__ldg(&p.part_lse[pi]) - m);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + pi * D) + c4);
+    const float w = exp2f(__ldg(&p.part_lse[lse0 + j * lse_step]) - m);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + o0 + j * o_step));
     wsum += w;
     acc.x = fmaf(w, v.x, acc.x);
     acc.y = fmaf(w, v.y, acc.y);
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
     acc.w = fmaf(w, v.w, acc.w);
   }
   const float inv = 1.f / wsum;
-  OutT* out = static_cast<OutT*>(p.out) + (int64_t(row) * p.H + h) * D + 4 * c4;
+  OutT* out = static_cast<OutT*>(p.out) + ((int64_t(s) * p.T + t) * p.H + h) * D + 4 * c4;
   if constexpr (sizeof(OutT) == 2) {
     __nv_bfloat162 a = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     __nv_bfloat162 b = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
@@ -170,9 +172,8 @@ __global__ void __launch_bounds__(256) attention_f32_kernel(const AttnParams p) 
     for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
   } else {
     const int64_t idx = (int64_t(split) * p.H + h) * p.T + t;
-    float* o = p.part_o + idx * D + lane * E;
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
+    for (int e = 0; e < E; ++e) p.part_o[part_o_offset<D>(split, h, t, lane * E + e, p.H, p.T)] = acc[e] * inv;
     if (lane == 0) p.part_lse[idx] = m + log2f(l);
   }
 }
