@@ -105,10 +105,10 @@ struct Cfg {
 __device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(kHalfKeys * (2 * t + b)); }
 
 // Trace mode (diagnostics): CTA 0 records the SM clock of an event for a chunk.
-__device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) {
-  if (p.trace != nullptr && blockIdx.x == 0 && chunk < p.trace_cap)
-    p.trace[int64_t(ev) * p.trace_cap + chunk] = clock64();
+__device__ __forceinline__ void trace_at(const AttnParams& p, int ev, int chunk, long long clk) {
+  if (p.trace != nullptr && blockIdx.x == 0 && chunk < p.trace_cap) p.trace[int64_t(ev) * p.trace_cap + chunk] = clk;
 }
+__device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) { trace_at(p, ev, chunk, clock64()); }
 
 __device__ __forceinline__ void signal_abort(int32_t* status, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -604,8 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ptx::tc_fence_before();
-        if (q4 == 0 && lane == 0) trace(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1);
+        // an arrive releases this thread's earlier writes, so the trace store follows it
+        const long long t_arrive = clock64();
         ptx::mbar_arrive(p_ready(t, b));
+        if (q4 == 0 && lane == 0) trace_at(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1, t_arrive);
       }
       if (!ok) signal_abort(p.status, abort_flag);
       if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
@@ -722,8 +724,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::fence_proxy_async_smem();  // P2 stores -> visible to the tensor core
         ptx::tc_fence_before();
-        if (q == 0 && lane == 0) trace(p, kTrP2Arrive, j);
+        const long long t_arrive = clock64();
         ptx::mbar_arrive(p2_ready(j & 1));
+        if (q == 0 && lane == 0) trace_at(p, kTrP2Arrive, j, t_arrive);
       }
       if (!ok) signal_abort(p.status, abort_flag);
       // this key group's (max, sum) of tail row `lane`
