@@ -495,6 +495,107 @@ def run_gpu(args, w: wl.Workload):
     return 0
 
 
+# ---------------------------------------------------------------- scale-phase prefill
+
+def run_prefill(args, w: wl.Workload):
+    """Scale phase ("Frame Processing Loop", num_frames > 1): a new stream's first F
+    frames are appended (all blocks) and then attend all of their F*T query rows over
+    the F frames at once, every block.  A step is one such prefill of one stream set,
+    on a cache reset before it; the inputs are resident in HBM."""
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist_init("nccl")
+    import streaming_paged_kv_two_gb300 as spk
+    from gpu_harness import spk_config_for, to_device
+
+    F, K, W = args.query_frames, args.steps, args.warmup
+    wk = w.replace(frames=F)
+    cfg, keep = spk_config_for(wk, args.splits, max_query_frames=F)
+    pool_bytes, ws_bytes = spk.required_bytes(cfg)
+    dev = torch.device("cuda", local)
+    pools = [torch.empty(pool_bytes, dtype=torch.uint8, device=dev) for _ in range(w.num_blocks)]
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    cache = spk.Cache(cfg, pools, keep)
+    stream = torch.cuda.current_stream()
+    B, L, T = w.num_streams, w.num_blocks, w.tokens_per_frame
+    kvs = [[[tuple(to_device(x, w.dtype) for x in wl.frame_kv(w, s, b, f)) for b in range(L)] for s in range(B)]
+           for f in range(F)]
+    qcat = [torch.cat([to_device(wl.frame_q(w, s, b, f), w.dtype) for s in range(B) for f in range(F)])
+            for b in range(L)]
+    outs = [torch.empty_like(qcat[b]) for b in range(L)]
+    ev_pairs = []
+
+    def prefill(timed_launches=False):
+        cache.reset()
+        for f in range(F):
+            for s in range(B):
+                k, v = kvs[f][s][0]
+                cache.append_frame(s, 0, k, v, stream)
+                cache.evict_frames(s)
+            for b in range(1, L):
+                for s in range(B):
+                    k, v = kvs[f][s][b]
+                    cache.append_frame(s, b, k, v, stream)
+        cache.plan_queries(F, ws, stream)
+        for b in range(L):
+            if timed_launches:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                cache.run_attention(b, qcat[b], outs[b], ws, stream)
+                e1.record(stream)
+                ev_pairs.append((e0, e1))
+            else:
+                cache.run_attention(b, qcat[b], outs[b], ws, stream)
+
+    for _ in range(W):
+        prefill()
+    info = cache.get_plan_info()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        prefill(timed_launches=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed = reduce_max(t0.elapsed_time(t1) / 1000.0, device=dev)
+    status = spk.read_device_status(ws, stream)
+    hbm, tflops, tflops_sus, peak_kind = load_peaks()
+    n_vis = visible_tokens(w, F)
+    Tq = F * T
+    flops = 4.0 * Tq * n_vis * w.num_heads * w.head_dim * B
+    byts = (2.0 * n_vis + 2.0 * Tq) * w.num_heads * w.head_dim * wl.element_bytes(w) * B
+    avg_launch = statistics.mean(a.elapsed_time(b) for a, b in ev_pairs) / 1000.0
+    achieved = flops / avg_launch / 1e12
+    line = {
+        "metric": f"scale-phase prefills/s ({F} frames, all blocks, 1 GB300)", "value": K * world / elapsed,
+        "unit": "prefills/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": elapsed / K * 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**workload_config(w, F), "workload": f"scale_phase_prefill_{F}x{T}", "query_rows": Tq,
+                   "l2": "no flush: each step rewrites the pools and reads them once"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                     "frac": achieved / tflops, "traffic": None,
+                     "kernel": "attention (tcgen05 paged attention), per block launch",
+                     "peak_source": f"{peak_kind} (bf16_tflops)", "avg_launch_us": avg_launch * 1e6,
+                     "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": byts,
+                     "frac_of_sustained": achieved / tflops_sus},
+        "gpu_launches": (F * B * L + L * (2 if info["merge_needed"] else 1)) * K,
+        "plan": info, "clocks": clk, "device_status": status,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    cache.close()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,6 +609,9 @@ def main(argv=None):
                     help="tuning only: force this many KV splits per stream (0 = the planner's choice)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="profiling only: override the block count (smaller device footprint)")
+    ap.add_argument("--query-frames", type=int, default=1,
+                    help="F > 1: time the scale-phase prefill (F frames appended, then F*T query rows "
+                         "attend over them) instead of the streaming step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "spk":
         args.warmup = 3
@@ -516,6 +620,8 @@ def main(argv=None):
         w = w.replace(num_blocks=args.blocks, name=f"{w.name}_blocks{args.blocks}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.query_frames > 1:
+        return run_prefill(args, w)
     return run_gpu(args, w)
 
 

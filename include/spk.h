@@ -83,7 +83,8 @@ typedef struct {
   int32_t max_special_pages;   /* MSP per stream, >= 1 (ceil(max_total_frames * S / ps)) */
   int32_t dtype;               /* enum spk_dtype */
   int32_t splits_per_stream;   /* 0 = planner's choice; k > 0 forces k KV splits per stream (clamped to [1, chunks]) */
-  int32_t reserved;            /* must be 0 */
+  int32_t max_query_frames;    /* most frames of queries one attention call may carry (spk_plan_queries);
+                                  0 or 1 = one frame per call.  Sizes the workspace's split partials. */
   const int32_t* patch_page_order;   /* optional host array [B*MPP]: initial free-list order, global ids;
                                         entries [s*MPP, (s+1)*MPP) must permute stream s's patch ids. NULL = ascending */
   const int32_t* special_page_order; /* optional host array [B*MSP], same rule for special ids. NULL = ascending */
@@ -152,6 +153,20 @@ int spk_evict_frames(spk_cache* cache, int stream);
  * stream must hold at least one frame.  A bookkeeping-only cache takes
  * workspace == NULL and builds the host tables only. */
 int spk_plan(spk_cache* cache, void* workspace, void* cuda_stream);
+
+/* Plan an attention call whose queries are the last `query_frames` frames of every
+ * stream: q and out then hold query_frames * T rows per stream (stream-major, the
+ * stream's frames oldest first, rows 0..P-1 patch and P..T-1 special within each
+ * frame), attending over the same visible keys as spk_plan.  This is the scale phase
+ * of "How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction"
+ * ("Frame Processing Loop": num_frames > 1): append and evict the initialisation
+ * frames one by one as usual, then one call attends every one of their query rows
+ * over all of them (full, non-causal attention over the frames).  Later in a stream
+ * the same call lets several recent frames query the whole visible cache at once.
+ * spk_plan(c, ws, s) is spk_plan_queries(c, 1, ws, s).  1 <= query_frames <=
+ * max(1, max_query_frames) and every stream must hold at least query_frames frames,
+ * else SPK_ERR_INVALID_ARG / SPK_ERR_BAD_STATE. */
+int spk_plan_queries(spk_cache* cache, int query_frames, void* workspace, void* cuda_stream);
 
 /* Attention of the current frame for one block, all streams in one launch.
  * q: device [B*T, H, D] (stream s owns rows s*T..s*T+T-1), out: device [B*T, H, D],

@@ -43,7 +43,7 @@ class spk_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_blocks", "num_streams", "num_heads", "head_dim", "page_size", "patches_per_frame",
         "specials_per_frame", "scale_frames", "sliding_window", "max_patch_pages", "max_special_pages",
-        "dtype", "splits_per_stream", "reserved")] + [
+        "dtype", "splits_per_stream", "max_query_frames")] + [
         ("patch_page_order", ctypes.POINTER(ctypes.c_int32)),
         ("special_page_order", ctypes.POINTER(ctypes.c_int32))]
 
@@ -73,6 +73,7 @@ def _load():
         "spk_append_frame": (I32, [P, I32, I32, P, P, P]),
         "spk_evict_frames": (I32, [P, I32]),
         "spk_plan": (I32, [P, P, P]),
+        "spk_plan_queries": (I32, [P, I32, P, P]),
         "spk_run_attention": (I32, [P, I32, P, P, P, P]),
         "spk_read_kv": (I32, [P, I32, I32, P, P]),
         "spk_get_plan_host": (I32, [P, pi32, ctypes.c_int32, pi32, pi32, pi32, pi32, pi32]),
@@ -122,11 +123,12 @@ def _stream(s):
 
 def make_config(*, num_blocks, num_streams, num_heads, head_dim, page_size, patches_per_frame,
                 specials_per_frame, scale_frames, sliding_window, max_patch_pages, max_special_pages,
-                dtype=SPK_BF16, splits_per_stream=0, patch_page_order=None, special_page_order=None):
+                dtype=SPK_BF16, splits_per_stream=0, patch_page_order=None, special_page_order=None,
+                max_query_frames=0):
     """Return (spk_config, keepalive) with the optional page orders as int32 host arrays."""
     c = spk_config(num_blocks, num_streams, num_heads, head_dim, page_size, patches_per_frame,
                    specials_per_frame, scale_frames, sliding_window, max_patch_pages, max_special_pages,
-                   dtype, splits_per_stream, 0)
+                   dtype, splits_per_stream, max_query_frames)
     keep = []
     for field, arr in (("patch_page_order", patch_page_order), ("special_page_order", special_page_order)):
         if arr is not None:
@@ -195,6 +197,9 @@ class Cache:
 
     def plan(self, workspace=None, cuda_stream=None):
         _check(lib.spk_plan(self._h, _ptr(workspace), _stream(cuda_stream)))
+
+    def plan_queries(self, query_frames: int, workspace=None, cuda_stream=None):
+        _check(lib.spk_plan_queries(self._h, int(query_frames), _ptr(workspace), _stream(cuda_stream)))
 
     def run_attention(self, block: int, q, out, workspace, cuda_stream=None):
         _check(lib.spk_run_attention(self._h, block, _ptr(q), _ptr(out), _ptr(workspace), _stream(cuda_stream)))

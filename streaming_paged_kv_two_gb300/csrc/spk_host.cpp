@@ -83,7 +83,8 @@ int validate_config(const spk_config* c) {
   if (c->max_patch_pages < 1 || c->max_special_pages < 1) return fail(SPK_ERR_INVALID_ARG, "max pages must be >= 1");
   if (c->dtype != SPK_BF16 && c->dtype != SPK_F32) return fail(SPK_ERR_INVALID_ARG, "dtype must be SPK_BF16 or SPK_F32");
   if (c->splits_per_stream < 0) return fail(SPK_ERR_INVALID_ARG, "splits_per_stream must be >= 0");
-  if (c->reserved != 0) return fail(SPK_ERR_INVALID_ARG, "reserved must be 0");
+  if (c->max_query_frames < 0 || c->max_query_frames > kMaxQueryFrames)
+    return fail(SPK_ERR_INVALID_ARG, "max_query_frames must be in [0, %d]", kMaxQueryFrames);
   int64_t pages = int64_t(c->num_streams) * (int64_t(c->max_patch_pages) + c->max_special_pages);
   if (pages > (int64_t(1) << 30)) return fail(SPK_ERR_INVALID_ARG, "too many pages");
   const int64_t B = c->num_streams, mpp = c->max_patch_pages, msp = c->max_special_pages;
@@ -119,8 +120,9 @@ WorkspaceLayout make_layout(const spk_config& c) {
   L.chunks = off;  off = align256(off + sizeof(ChunkDesc) * L.max_chunks);
   L.works = off;   off = align256(off + sizeof(WorkDesc) * L.max_splits);
   L.plan_end = off;
-  L.part_o = off;  off = align256(off + sizeof(float) * size_t(L.max_splits) * c.num_heads * T * c.head_dim);
-  L.part_lse = off; off = align256(off + sizeof(float) * size_t(L.max_splits) * c.num_heads * T);
+  const int64_t Tq = T * std::max(1, c.max_query_frames);  // query rows per stream of the largest plan
+  L.part_o = off;  off = align256(off + sizeof(float) * size_t(L.max_splits) * c.num_heads * Tq * c.head_dim);
+  L.part_lse = off; off = align256(off + sizeof(float) * size_t(L.max_splits) * c.num_heads * Tq);
   L.total = off;
   return L;
 }
@@ -147,7 +149,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 struct spk_cache {
   spk_config cfg{};
   bool dry = true;
-  int T = 0;
+  int T = 0;   // rows of one frame (P + S)
+  int Tq = 0;  // query rows per stream of the current plan (query_frames * T)
   int device = 0;
   int num_sms = 152;
   std::vector<void*> pools;
@@ -250,10 +253,10 @@ int choose_splits(const spk_cache* c, const std::vector<int32_t>& nchunks, std::
   for (int s = 0; s < B; ++s) cmax = std::max(cmax, nchunks[s]);
   int per_split_ctas, slots;
   if (g.dtype == SPK_BF16) {
-    per_split_ctas = B * g.num_heads * attention_bf16_tiles(c->T, g.head_dim).ngroups;
+    per_split_ctas = B * g.num_heads * attention_bf16_tiles(c->Tq, g.head_dim).ngroups;
     slots = c->num_sms;
   } else {
-    per_split_ctas = B * g.num_heads * ((c->T + 7) / 8);
+    per_split_ctas = B * g.num_heads * ((c->Tq + 7) / 8);
     slots = c->num_sms * 8;
   }
   const double overhead_chunks = 2.0, split_charge = 0.25;
@@ -292,7 +295,7 @@ int build_plan(spk_cache* c) {
     c->kv_indptr.push_back(c->kv_indptr.back() + int32_t(pages.size()));
     c->lpl.push_back(last_len);
     c->npp.push_back(np);
-    c->qo.push_back(c->qo.back() + c->T);
+    c->qo.push_back(c->qo.back() + c->Tq);
     chunk_base[s] = int32_t(c->chunks.size());
     for (size_t i = 0; i < pages.size(); ++i) {
       int32_t ntok;
@@ -324,7 +327,7 @@ int build_plan(spk_cache* c) {
   c->info.num_chunks = int32_t(c->chunks.size());
   c->info.num_splits = int32_t(c->works.size());
   c->info.num_ctas = int32_t(c->works.size()) * g.num_heads *
-                     (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->T, g.head_dim).ngroups : (c->T + 7) / 8);
+                     (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->Tq, g.head_dim).ngroups : (c->Tq + 7) / 8);
   c->info.merge_needed = merge ? 1 : 0;
   c->info.visible_tokens = visible;
   return SPK_OK;
@@ -378,6 +381,7 @@ int spk_create_cache(const spk_config* cfg, void* const* pools, spk_cache** out)
   c->cfg.patch_page_order = nullptr;
   c->cfg.special_page_order = nullptr;
   c->T = cfg->patches_per_frame + cfg->specials_per_frame;
+  c->Tq = c->T;
   c->ws = make_layout(c->cfg);
   const int B = cfg->num_streams;
   const int32_t mpp = cfg->max_patch_pages, msp = cfg->max_special_pages;
@@ -513,19 +517,30 @@ int spk_evict_frames(spk_cache* c, int stream) {
   return ok();
 }
 
-int spk_plan(spk_cache* c, void* workspace, void* cuda_stream) {
+int spk_plan_queries(spk_cache* c, int query_frames, void* workspace, void* cuda_stream) {
   int rc = check_cache(c);
   if (rc) return rc;
   if (c->dry && workspace) return fail(SPK_ERR_INVALID_ARG, "bookkeeping-only cache takes workspace = NULL");
   if (!c->dry && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255)))
     return fail(SPK_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  const int max_qf = std::max(1, c->cfg.max_query_frames);
+  if (query_frames < 1 || query_frames > max_qf)
+    return fail(SPK_ERR_INVALID_ARG, "query_frames %d outside [1, %d] (spk_config.max_query_frames)", query_frames,
+                max_qf);
+  for (int s = 0; s < c->cfg.num_streams; ++s)
+    if (c->st[s].frame_count < query_frames)
+      return fail(SPK_ERR_BAD_STATE, "stream %d holds %lld frames, fewer than the %d query frames", s,
+                  (long long)c->st[s].frame_count, query_frames);
   c->plan_valid = false;
+  c->Tq = query_frames * c->T;
   if ((rc = build_plan(c))) return rc;
   if (!c->dry && (rc = upload_plan(c, workspace, static_cast<cudaStream_t>(cuda_stream)))) return rc;
   c->plan_ws = workspace;
   c->plan_valid = true;
   return ok();
 }
+
+int spk_plan(spk_cache* c, void* workspace, void* cuda_stream) { return spk_plan_queries(c, 1, workspace, cuda_stream); }
 
 }  // extern "C"
 
@@ -549,14 +564,14 @@ AttnParams attention_params(const spk_cache* c, int block, const void* q, void* 
   p.row_stride = int64_t(g.num_heads) * g.head_dim;
   p.half_stride = int64_t(g.page_size) * p.row_stride;
   p.page_stride = 2 * p.half_stride;
-  p.T = c->T;
+  p.T = c->Tq;
   p.H = g.num_heads;
   p.D = g.head_dim;
   p.ps = g.page_size;
   p.num_splits = c->info.num_splits;
-  p.ntiles = (c->T + kTileRows - 1) / kTileRows;
+  p.ntiles = (c->Tq + kTileRows - 1) / kTileRows;
   {
-    const TileShape ts = attention_bf16_tiles(c->T, g.head_dim);
+    const TileShape ts = attention_bf16_tiles(c->Tq, g.head_dim);
     p.main_tiles = ts.main_tiles;
     p.tail_rows = ts.tail_rows;
     p.ngroups = ts.ngroups;
@@ -580,7 +595,7 @@ int launch_attention(const spk_cache* c, int block, const AttnParams& p, char* w
     m.streams = reinterpret_cast<const StreamDesc*>(ws + c->ws.streams);
     m.out = p.out;
     m.B = g.num_streams;
-    m.T = c->T;
+    m.T = c->Tq;
     m.H = g.num_heads;
     m.D = g.head_dim;
     e = launch_merge(m, g.dtype, stream);
@@ -652,7 +667,7 @@ int spk_run_attention_static_scratch(spk_cache* c, int block, const void* q, voi
     if (!c->st[s].appended[block])
       return fail(SPK_ERR_BAD_STATE, "block %d of stream %d not appended in the current frame", block, s);
   // partials of every split: fp32 O [splits][H][T][D], then fp32 lse [splits][H][T] (256-byte aligned)
-  const size_t rows = size_t(c->info.num_splits) * g.num_heads * c->T;
+  const size_t rows = size_t(c->info.num_splits) * g.num_heads * c->Tq;
   const size_t o_bytes = align256(rows * g.head_dim * sizeof(float));
   const size_t need = o_bytes + rows * sizeof(float);
   if (need > static_scratch_bytes())

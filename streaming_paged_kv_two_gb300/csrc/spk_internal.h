@@ -16,6 +16,8 @@ constexpr int kChunkTokens = 128;
 constexpr int kMaxSplitsPerStream = 32;
 // Special rows per frame that one append carries in its kernel parameters.
 constexpr int kMaxSpecials = 64;
+// Upper bound of spk_config.max_query_frames (frames of queries in one attention call).
+constexpr int kMaxQueryFrames = 64;
 // Query rows per tensor-core tile (tcgen05 M).
 constexpr int kTileRows = 128;
 // Events recorded by the bf16 attention kernel's trace mode (per chunk, CTA 0).

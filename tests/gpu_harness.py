@@ -13,14 +13,14 @@ BF16_MEAN_ABS = 2e-3
 F32_MAX_ABS = 1e-4
 
 
-def spk_config_for(w: wl.Workload, splits: int = 0):
+def spk_config_for(w: wl.Workload, splits: int = 0, max_query_frames: int = 0):
     po, so = wl.page_orders(w)
     return spk.make_config(
         num_blocks=w.num_blocks, num_streams=w.num_streams, num_heads=w.num_heads, head_dim=w.head_dim,
         page_size=w.page_size, patches_per_frame=w.patches_per_frame, specials_per_frame=w.specials_per_frame,
         scale_frames=w.scale_frames, sliding_window=w.sliding_window, max_patch_pages=w.max_patch_pages,
         max_special_pages=w.max_special_pages, dtype=spk.SPK_BF16 if w.dtype == "bf16" else spk.SPK_F32,
-        splits_per_stream=splits,
+        splits_per_stream=splits, max_query_frames=max_query_frames,
         patch_page_order=None if po is None else po.tolist(),
         special_page_order=None if so is None else so.tolist())
 
@@ -40,9 +40,9 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 class Harness:
     """Pools, workspace and an spk cache on cuda:0 for one workload."""
 
-    def __init__(self, w: wl.Workload, splits: int = 0):
+    def __init__(self, w: wl.Workload, splits: int = 0, max_query_frames: int = 0):
         self.w = w
-        self.cfg, self.keep = spk_config_for(w, splits)
+        self.cfg, self.keep = spk_config_for(w, splits, max_query_frames)
         pool_bytes, ws_bytes = spk.required_bytes(self.cfg)
         self.pools = [torch.empty(pool_bytes, dtype=torch.uint8, device="cuda") for _ in range(w.num_blocks)]
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
@@ -61,6 +61,9 @@ class Harness:
 
     def plan(self):
         self.cache.plan(self.ws, self.stream)
+
+    def plan_queries(self, query_frames: int):
+        self.cache.plan_queries(query_frames, self.ws, self.stream)
 
     def run(self, block: int, q: np.ndarray) -> np.ndarray:
         qd = to_device(q, self.w.dtype)

@@ -259,3 +259,58 @@ def test_split_choice_is_valid():
         info = c.get_plan_info()
         assert info["num_splits"] == min(k, 32, info["num_chunks"])
         assert info["merge_needed"] == (1 if info["num_splits"] > 1 else 0)
+
+
+# ------------------------------------------------------------------ several frames of queries
+
+def test_plan_queries_tables_and_errors():
+    """Scale-phase prefill plan ("Frame Processing Loop", num_frames > 1): the visible
+    table is that of spk_plan, the query rows per stream are query_frames * T."""
+    w = wl.CONFIGS[3].replace(frames=64)
+    cfg, keep = cfg_for(w, max_query_frames=8)
+    c = spk.Cache(cfg, None, keep)
+    T = w.tokens_per_frame
+    with pytest.raises(spk.SpkError) as e:
+        c.plan_queries(1)                       # no frame yet
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    for f in range(8):
+        c.append_frame(0, 0); c.evict_frames(0)
+    c.plan()
+    one = c.get_plan_host()
+    for qf in (1, 2, 8):
+        c.plan_queries(qf)
+        got = c.get_plan_host()
+        for key in ("indices", "kv_indptr", "last_page_len", "num_patch_pages"):
+            assert np.array_equal(got[key], one[key]), key
+        assert list(got["qo_indptr"]) == [0, qf * T]
+        info = c.get_plan_info()
+        rows = qf * T
+        main, rem = divmod(rows, 128)
+        if rem > 8:                             # more than the D = 64 tail holds: another 128-row tile
+            main += 1
+        groups = max(1, -(-main // 2))          # two main tiles per CTA
+        assert info["num_ctas"] == info["num_splits"] * w.num_heads * groups
+    for bad in (0, 9):
+        with pytest.raises(spk.SpkError) as e:
+            c.plan_queries(bad)
+        assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    cfg1, keep1 = cfg_for(w)                    # max_query_frames = 0: one frame per call
+    c1 = spk.Cache(cfg1, None, keep1)
+    c1.append_frame(0, 0); c1.append_frame(0, 0)
+    with pytest.raises(spk.SpkError) as e:
+        c1.plan_queries(2)
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG
+    c2 = spk.Cache(cfg, None, keep)
+    c2.append_frame(0, 0)
+    with pytest.raises(spk.SpkError) as e:
+        c2.plan_queries(2)                      # only one frame held
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+
+
+def test_max_query_frames_sizes_the_workspace():
+    w = wl.CONFIGS[3]
+    ws = [spk.required_bytes(cfg_for(w, max_query_frames=q)[0])[1] for q in (0, 1, 8)]
+    assert ws[0] == ws[1] < ws[2]
+    with pytest.raises(spk.SpkError) as e:
+        spk.required_bytes(cfg_for(w, max_query_frames=65)[0])
+    assert e.value.code == spk.SPK_ERR_INVALID_ARG and "max_query_frames" in str(e.value)

@@ -222,6 +222,58 @@ def test_stream_parity(name):
     print(f"{name}: worst max-abs {worst[0]:.3e} mean-abs {worst[1]:.3e}")
 
 
+# ------------------------------------------------------------------ several frames of queries
+
+def queries_and_check(w: wl.Workload, plans: dict, splits: int = 0):
+    """Stream w.frames frames; after frame f (all blocks appended), when f is in plans,
+    plan plans[f] frames of queries and compare every block's output, whose rows are
+    the last plans[f] frames' queries of each stream, with the oracle."""
+    gh = _h()
+    h = gh.Harness(w, splits, max_query_frames=max(plans.values()))
+    streams = make_streams(w)
+    fetch_cache = {}
+    for f in range(w.frames):
+        for s in range(w.num_streams):
+            h.append(s, 0, *wl.frame_kv(w, s, 0, f))
+            streams[s].append()
+        for s in range(w.num_streams):
+            h.cache.evict_frames(s)
+            streams[s].evict()
+        h.plan()
+        for b in range(1, w.num_blocks):
+            for s in range(w.num_streams):
+                h.append(s, b, *wl.frame_kv(w, s, b, f))
+        if f not in plans:
+            continue
+        qf = plans[f]
+        h.plan_queries(qf)
+        for b in range(w.num_blocks):
+            qs = [np.concatenate([wl.frame_q(w, s, b, g) for g in range(f - qf + 1, f + 1)])
+                  for s in range(w.num_streams)]
+            got = h.run(b, np.concatenate(qs))
+            fetchers = [frame_fetcher(w, s, b, fetch_cache.setdefault((s, b), {})) for s in range(w.num_streams)]
+            want = np.concatenate([
+                oracle.attend(wl.to_f64(qs[s], w.dtype), *oracle.gather_visible(streams[s].visible_sources(),
+                                                                                 fetchers[s]))[0]
+                for s in range(w.num_streams)])
+            gh.check_close(got, want, w.dtype, f"{w.name} frame {f} block {b}, {qf} query frames")
+    assert h.status() == 0
+    h.close()
+
+
+@pytest.mark.parametrize("name,w,plans,splits", [
+    # scale phase: the first frames, full attention over all of them (8 x 262 = 2096 rows)
+    ("scale_phase_d64", small(scale_frames=8, sliding_window=4, frames=8), {7: 8}, 0),
+    ("scale_phase_d64_split3", small(scale_frames=4, sliding_window=2, frames=4), {3: 4}, 3),
+    ("midstream_d128_two_streams", small(head_dim=128, num_streams=2, shuffle_pages=True, frames=7), {6: 3}, 2),
+    ("midstream_f32", small(dtype="f32", frames=6, value_scale=1.0), {2: 2, 5: 3}, 2),
+    ("tail_only_d64", small(patches_per_frame=2, specials_per_frame=1, page_size=16, frames=5), {4: 2}, 0),
+    ("t130_x2_tail_d64", small(patches_per_frame=124, frames=4), {3: 2}, 2),
+])
+def test_multi_frame_query_parity(name, w, plans, splits):
+    queries_and_check(w.replace(name=name), plans, splits)
+
+
 # ------------------------------------------------------------------ state errors on a real cache
 
 def test_run_attention_state_errors():
