@@ -146,6 +146,26 @@ int spk_append_frame(spk_cache* cache, int stream, int block, const void* k, con
  * sliding_window remain.  Host only, no data moves.  Marks the plan stale. */
 int spk_evict_frames(spk_cache* cache, int stream);
 
+/* Deferred eviction ("How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D
+ * Reconstruction", "Scale Frames vs Sliding Window": deferred eviction for algorithms
+ * that roll frames back, such as key-frame selection).  While on, spk_evict_frames
+ * leaves the stream's live window as it is, so the window may hold more than
+ * sliding_window frames (all visible) and no page is recycled; turning it off
+ * changes nothing by itself, the next spk_evict_frames applies the window rule
+ * (oldest pages first).  Host only.  Off after create and reset. */
+int spk_set_defer_eviction(spk_cache* cache, int stream, int on);
+
+/* Roll back the stream's newest frame: the bookkeeping returns to its state just
+ * before that frame's append(block 0) -- its patch page goes back to the front of
+ * the free list, the special pages it opened to the front of the free special
+ * list, its S special tokens are dropped, the frame count and the previous frame's
+ * block-append marks are restored -- so the next append takes the same targets
+ * again.  The pool data is not touched (the rolled-back slots are no longer
+ * visible).  One rollback per append; SPK_ERR_BAD_STATE when nothing was appended
+ * since the last rollback or reset, or when the frame's patch page was already
+ * evicted (defer eviction to keep it).  Marks the plan stale.  Host only. */
+int spk_rollback_frame(spk_cache* cache, int stream);
+
 /* Plan the current frame for every stream: visible page table, indptr,
  * last_page_len, patch-page counts, KV chunks and the split-KV work list.  Built on
  * the host and uploaded with one async copy into `workspace` on cuda_stream; the

@@ -24,6 +24,7 @@ which print none.
 from .paged_cache import (  # noqa: F401
     OutOfPatchPages,
     OutOfSpecialPages,
+    RollbackUnavailable,
     StreamPages,
     default_page_ids,
     plan,

@@ -25,12 +25,21 @@ Sources (page title, section):
 * "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback in
   Streaming Inference", "Inspecting Cache Statistics": the statistics dict
   (frame_count, scale_pages, live_pages, free_pages, special_tokens).
+* "How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction",
+  "Scale Frames vs Sliding Window" and "Summary": deferred eviction, so that a
+  frame can be rolled back (key-frame selection) without losing cache contents.
 
 Readings where the pages are silent: the free lists are FIFO (allocate from the
 front, recycle to the back); the initial order is ascending unless an explicit
 order is given; an append that cannot get every page it needs changes nothing;
 last_page_len is in [1, page_size], never 0; with several streams, stream s owns
 patch ids [s*MPP, (s+1)*MPP) and special ids [B*MPP + s*MSP, B*MPP + (s+1)*MSP).
+Deferred eviction and rollback (the pages name the feature only): while deferral is
+on, evict() keeps the live window as it is; rollback() removes the newest frame and
+returns the bookkeeping to its state just before that frame's append -- its patch
+page goes back to the front of the free list, the special pages it opened to the
+front of the free special list, its special tokens are dropped.  One rollback per
+append; it needs the frame's patch page still held (not already evicted).
 """
 from __future__ import annotations
 
@@ -42,6 +51,10 @@ class OutOfPatchPages(RuntimeError):
 
 
 class OutOfSpecialPages(RuntimeError):
+    pass
+
+
+class RollbackUnavailable(RuntimeError):
     pass
 
 
@@ -72,6 +85,8 @@ class StreamPages:
         self.special_pages: list[int] = []                     # all_special_pages
         self.special_tokens = 0
         self.frame_count = 0
+        self.defer = False          # deferred eviction
+        self.undo = None            # what the newest append took, while it can be rolled back
         # provenance of every written slot: page -> {slot: (frame, row of that frame)}
         self.contents: dict[int, dict[int, tuple[int, int]]] = {}
 
@@ -91,10 +106,12 @@ class StreamPages:
 
         f = self.frame_count
         pid = self.free.popleft()
-        if len(self.scale) < self.sc:
+        in_scale = len(self.scale) < self.sc
+        if in_scale:
             self.scale.append(pid)
         else:
             self.live.append(pid)
+        opened = []
         page = self.contents.setdefault(pid, {})
         for t in range(self.P):
             page[t] = (f, t)
@@ -104,19 +121,49 @@ class StreamPages:
             pos = first + j
             if pos // self.ps == len(self.special_pages):
                 self.special_pages.append(self.special_free.popleft())
+                opened.append(self.special_pages[-1])
             sp = self.special_pages[pos // self.ps]
             slot = pos % self.ps
             self.contents.setdefault(sp, {})[slot] = (f, self.P + j)
             targets.append((sp, slot))
         self.special_tokens += self.S
         self.frame_count += 1
+        self.undo = (pid, in_scale, opened, targets)
         return pid, targets
 
     # -- evict_frames -------------------------------------------------------
     def evict(self):
-        """Return the oldest live-window pages to the free list until the window fits."""
+        """Return the oldest live-window pages to the free list until the window fits
+        (nothing while eviction is deferred)."""
+        if self.defer:
+            return
         while len(self.live) > self.w:
             self.free.append(self.live.popleft())
+
+    # -- deferred eviction and rollback ---------------------------------------
+    def set_defer(self, on: bool):
+        self.defer = bool(on)
+
+    def rollback(self):
+        """Remove the newest frame: the state returns to just before its append."""
+        if self.undo is None:
+            raise RollbackUnavailable("no frame to roll back since the last append")
+        pid, in_scale, opened, targets = self.undo
+        held = self.scale if in_scale else self.live
+        if not held or held[-1] != pid:
+            raise RollbackUnavailable("the newest frame's patch page was already evicted")
+        held.pop()
+        self.free.appendleft(pid)
+        self.contents.pop(pid, None)
+        for sp, slot in targets:
+            del self.contents[sp][slot]
+        for sp in reversed(opened):
+            assert self.special_pages[-1] == sp
+            self.special_pages.pop()
+            self.special_free.appendleft(sp)
+        self.special_tokens -= self.S
+        self.frame_count -= 1
+        self.undo = None
 
     # -- plan pieces ----------------------------------------------------------
     def visible_pages(self) -> list[int]:

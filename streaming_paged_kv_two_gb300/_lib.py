@@ -73,6 +73,8 @@ def _load():
         "spk_append_frame": (I32, [P, I32, I32, P, P, P]),
         "spk_evict_frames": (I32, [P, I32]),
         "spk_plan": (I32, [P, P, P]),
+        "spk_set_defer_eviction": (I32, [P, I32, I32]),
+        "spk_rollback_frame": (I32, [P, I32]),
         "spk_plan_queries": (I32, [P, I32, P, P]),
         "spk_run_attention": (I32, [P, I32, P, P, P, P]),
         "spk_read_kv": (I32, [P, I32, I32, P, P]),
@@ -197,6 +199,12 @@ class Cache:
 
     def plan(self, workspace=None, cuda_stream=None):
         _check(lib.spk_plan(self._h, _ptr(workspace), _stream(cuda_stream)))
+
+    def set_defer_eviction(self, stream: int, on: bool):
+        _check(lib.spk_set_defer_eviction(self._h, stream, 1 if on else 0))
+
+    def rollback_frame(self, stream: int):
+        _check(lib.spk_rollback_frame(self._h, stream))
 
     def plan_queries(self, query_frames: int, workspace=None, cuda_stream=None):
         _check(lib.spk_plan_queries(self._h, int(query_frames), _ptr(workspace), _stream(cuda_stream)))

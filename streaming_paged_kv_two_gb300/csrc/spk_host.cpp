@@ -62,6 +62,17 @@ struct StreamState {
   std::vector<int32_t> cur_spage, cur_sslot;
   std::vector<uint8_t> appended;      // per block: appended in the current frame
   std::vector<int32_t> init_patch, init_special;
+  bool defer_eviction = false;        // evict_frames leaves the live window as it is
+  // What the newest append took, kept until the next append, a rollback or a reset.
+  struct Undo {
+    bool valid = false;
+    int32_t pid = -1;
+    bool in_scale = false;
+    std::vector<int32_t> opened;      // special pages the frame opened, in order
+    int32_t prev_patch = -1;
+    std::vector<int32_t> prev_spage, prev_sslot;
+    std::vector<uint8_t> prev_appended;
+  } undo;
 };
 
 int elem_bytes(int dtype) { return dtype == SPK_BF16 ? 2 : 4; }
@@ -189,6 +200,8 @@ void reset_state(spk_cache* c) {
     s.cur_spage.assign(g.specials_per_frame, -1);
     s.cur_sslot.assign(g.specials_per_frame, -1);
     s.appended.assign(g.num_blocks, 0);
+    s.defer_eviction = false;
+    s.undo = StreamState::Undo{};
   }
   c->plan_valid = false;
   c->plan_ws = nullptr;
@@ -217,9 +230,18 @@ int allocate_frame(spk_cache* c, StreamState& s) {
   const int64_t need = last / g.page_size + 1 - int64_t(s.special_pages.size());
   if (need > int64_t(s.special_free.size()))
     return fail(SPK_ERR_OUT_OF_SPECIAL_PAGES, "special page pool exhausted after %lld special tokens", (long long)first);
+  StreamState::Undo& u = s.undo;
+  u.valid = true;
+  u.prev_patch = s.cur_patch;
+  u.prev_spage = s.cur_spage;
+  u.prev_sslot = s.cur_sslot;
+  u.prev_appended = s.appended;
+  u.opened.clear();
   const int32_t pid = s.free_patch.front();
   s.free_patch.pop_front();
-  if (int64_t(s.scale.size()) < g.scale_frames) s.scale.push_back(pid);
+  u.pid = pid;
+  u.in_scale = int64_t(s.scale.size()) < g.scale_frames;
+  if (u.in_scale) s.scale.push_back(pid);
   else s.live.push_back(pid);
   s.cur_patch = pid;
   for (int j = 0; j < g.specials_per_frame; ++j) {
@@ -227,6 +249,7 @@ int allocate_frame(spk_cache* c, StreamState& s) {
     if (pos / g.page_size == int64_t(s.special_pages.size())) {
       s.special_pages.push_back(s.special_free.front());
       s.special_free.pop_front();
+      u.opened.push_back(s.special_pages.back());
     }
     s.cur_spage[j] = s.special_pages[pos / g.page_size];
     s.cur_sslot[j] = int32_t(pos % g.page_size);
@@ -509,10 +532,49 @@ int spk_evict_frames(spk_cache* c, int stream) {
   if (rc) return rc;
   if ((rc = check_stream(c, stream))) return rc;
   StreamState& s = c->st[stream];
-  while (int64_t(s.live.size()) > c->cfg.sliding_window) {
+  while (!s.defer_eviction && int64_t(s.live.size()) > c->cfg.sliding_window) {
     s.free_patch.push_back(s.live.front());
     s.live.pop_front();
   }
+  c->plan_valid = false;
+  return ok();
+}
+
+int spk_set_defer_eviction(spk_cache* c, int stream, int on) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if ((rc = check_stream(c, stream))) return rc;
+  c->st[stream].defer_eviction = on != 0;
+  return ok();
+}
+
+int spk_rollback_frame(spk_cache* c, int stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if ((rc = check_stream(c, stream))) return rc;
+  const spk_config& g = c->cfg;
+  StreamState& s = c->st[stream];
+  StreamState::Undo& u = s.undo;
+  if (!u.valid) return fail(SPK_ERR_BAD_STATE, "stream %d: no frame to roll back since its last append", stream);
+  const bool held = u.in_scale ? (!s.scale.empty() && s.scale.back() == u.pid)
+                               : (!s.live.empty() && s.live.back() == u.pid);
+  if (!held)
+    return fail(SPK_ERR_BAD_STATE, "stream %d: the newest frame's patch page was already evicted "
+                "(defer eviction to keep frames that may be rolled back)", stream);
+  if (u.in_scale) s.scale.pop_back();
+  else s.live.pop_back();
+  s.free_patch.push_front(u.pid);
+  for (auto it = u.opened.rbegin(); it != u.opened.rend(); ++it) {
+    s.special_pages.pop_back();
+    s.special_free.push_front(*it);
+  }
+  s.special_tokens -= g.specials_per_frame;
+  s.frame_count -= 1;
+  s.cur_patch = u.prev_patch;
+  s.cur_spage = u.prev_spage;
+  s.cur_sslot = u.prev_sslot;
+  s.appended = u.prev_appended;
+  u.valid = false;
   c->plan_valid = false;
   return ok();
 }

@@ -314,3 +314,87 @@ def test_max_query_frames_sizes_the_workspace():
     with pytest.raises(spk.SpkError) as e:
         spk.required_bytes(cfg_for(w, max_query_frames=65)[0])
     assert e.value.code == spk.SPK_ERR_INVALID_ARG and "max_query_frames" in str(e.value)
+
+
+# ------------------------------------------------------------------ deferred eviction and rollback
+
+def _op_sequence_matches_oracle(w: wl.Workload, ops: int, seed: int):
+    """Seeded random append / evict / defer / rollback / plan sequence: the library's
+    tables, statistics and frame targets equal the oracle's after every step."""
+    cfg, keep = cfg_for(w)
+    cache = spk.Cache(cfg, None, keep)
+    streams = make_streams(w)
+    rng = np.random.default_rng(seed)
+    T = w.tokens_per_frame
+    rolled = 0
+    for i in range(ops):
+        s = int(rng.integers(w.num_streams))
+        st = streams[s]
+        r = rng.random()
+        if r < 0.45:
+            try:
+                want = st.append()
+            except (oracle.OutOfPatchPages, oracle.OutOfSpecialPages):
+                with pytest.raises(spk.SpkError):
+                    cache.append_frame(s, 0)
+                continue
+            cache.append_frame(s, 0)
+            assert cache.get_frame_targets(s) == want, i
+        elif r < 0.65:
+            st.evict()
+            cache.evict_frames(s)
+        elif r < 0.75:
+            on = bool(rng.integers(2))
+            st.set_defer(on)
+            cache.set_defer_eviction(s, on)
+        else:
+            try:
+                st.rollback()
+            except oracle.RollbackUnavailable:
+                with pytest.raises(spk.SpkError) as e:
+                    cache.rollback_frame(s)
+                assert e.value.code == spk.SPK_ERR_BAD_STATE
+                continue
+            cache.rollback_frame(s)
+            rolled += 1
+        assert cache.get_stats(s) == st.stats(), i
+        if all(x.frame_count for x in streams):
+            cache.plan()
+            assert cache.get_plan_host() == oracle.plan(streams, T), i
+    cache.close()
+    assert rolled > 0
+
+
+@pytest.mark.parametrize("over,seed", [
+    (dict(), 1),
+    (dict(scale_frames=2, sliding_window=3), 2),
+    (dict(scale_frames=0, sliding_window=0), 3),
+    (dict(page_size=16, patches_per_frame=16, specials_per_frame=6, sliding_window=2, scale_frames=1), 4),
+    (dict(num_streams=3, shuffle_pages=True, sliding_window=4, scale_frames=2), 5),
+])
+def test_rollback_and_deferral_match_oracle(over, seed):
+    w = wl.CONFIGS[2].replace(frames=120, num_blocks=2, **over)
+    _op_sequence_matches_oracle(w, 600, seed)
+
+
+def test_rollback_restores_block_marks_and_targets():
+    c = _dry()                                   # 3 blocks
+    c.set_defer_eviction(0, True)
+    c.append_frame(0, 0); c.append_frame(0, 1); c.append_frame(0, 2)
+    prev = c.get_frame_targets(0)
+    c.append_frame(0, 0)                         # new frame: only block 0 so far
+    new = c.get_frame_targets(0)
+    c.rollback_frame(0)
+    assert c.get_frame_targets(0) == prev
+    with pytest.raises(spk.SpkError) as e:
+        c.append_frame(0, 1)                     # block 1 of the restored frame was already appended
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    with pytest.raises(spk.SpkError) as e:
+        c.rollback_frame(0)                      # one rollback per append
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    c.append_frame(0, 0)
+    assert c.get_frame_targets(0) == new         # the same targets again
+    c.reset()
+    with pytest.raises(spk.SpkError) as e:
+        c.rollback_frame(0)
+    assert e.value.code == spk.SPK_ERR_BAD_STATE

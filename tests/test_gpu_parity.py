@@ -274,6 +274,58 @@ def test_multi_frame_query_parity(name, w, plans, splits):
     queries_and_check(w.replace(name=name), plans, splits)
 
 
+# ------------------------------------------------------------------ deferred eviction and rollback
+
+def test_rolled_back_frame_is_not_visible():
+    """Key-frame selection: a candidate frame is appended with eviction deferred, attended,
+    rolled back and replaced by another frame; attention then sees the replacement and
+    the frame the deferral kept in the window, never the candidate."""
+    gh = _h()
+    w = small(frames=9, scale_frames=1, sliding_window=2, num_blocks=2)
+    h = gh.Harness(w, splits=2)
+    streams = make_streams(w)
+    st = streams[0]
+    T = w.tokens_per_frame
+    caches = {}
+
+    def check(f, data_frame, alias):
+        for b in range(w.num_blocks):
+            q = wl.frame_q(w, 0, b, data_frame)
+            got = h.run(b, q)
+            base = frame_fetcher(w, 0, b, caches.setdefault((b, data_frame != f), {}))
+            fetch = lambda frame, rows: base(alias.get(frame, frame), rows)   # noqa: E731
+            want = oracle.attend(wl.to_f64(q, w.dtype), *oracle.gather_visible(st.visible_sources(), fetch))[0]
+            gh.check_close(got, want, w.dtype, f"frame {f} block {b} (data of frame {data_frame})")
+
+    def append_all(f, data_frame, defer=None):
+        h.append(0, 0, *wl.frame_kv(w, 0, 0, data_frame))
+        st.append()
+        if defer is not None:
+            h.cache.set_defer_eviction(0, defer)
+            st.set_defer(defer)
+        h.cache.evict_frames(0)
+        st.evict()
+        h.plan()
+        for b in range(1, w.num_blocks):
+            h.append(0, b, *wl.frame_kv(w, 0, b, data_frame))
+
+    for f in range(w.frames):
+        if f in (4, 7):
+            cand = 1000 + f
+            h.cache.set_defer_eviction(0, True)
+            st.set_defer(True)
+            append_all(f, cand)
+            check(f, cand, {f: cand})              # the candidate is visible while pending
+            h.cache.rollback_frame(0)
+            st.rollback()
+            append_all(f, f, defer=False)          # the replacement; deferral ends with its eviction
+        else:
+            append_all(f, f)
+        check(f, f, {})
+    assert h.status() == 0
+    h.close()
+
+
 # ------------------------------------------------------------------ state errors on a real cache
 
 def test_run_attention_state_errors():

@@ -9,6 +9,10 @@
 * closed forms of attention (equal keys, one dominant key, V scaling, key shift);
 * the log-sum-exp merge equals attention over the union, and lse equals a library
   logsumexp of the logits;
+* deferred eviction and rollback: a rolled-back frame leaves the bookkeeping
+  exactly as before its append (and the next append takes the same targets);
+  deferred evictions, once committed, give the visible frames of a stream that
+  never deferred;
 * planted mistakes in the oracle are caught by at least one of the pins above.
 """
 from __future__ import annotations
@@ -224,6 +228,40 @@ def pin_merge(seed=3):
     np.testing.assert_allclose(o, full_o, atol=1e-14)
 
 
+def _state(st):
+    return (list(st.free), list(st.scale), list(st.live), list(st.special_free), list(st.special_pages),
+            st.special_tokens, st.frame_count, st.visible_sources() if st.frame_count else [])
+
+
+def pin_rollback(cfg):
+    """Rollback restores the pre-append state; committed deferrals match plain eviction."""
+    st = make_streams(cfg)[0]
+    ref = make_streams(cfg)[0]
+    st.set_defer(True)
+    for f in range(cfg.frames - 1):
+        before = _state(st)
+        first = st.append()
+        st.evict()                              # deferred: a no-op
+        st.rollback()
+        assert _state(st) == before, f"rollback at frame {f} did not restore the state"
+        assert st.append() == first, "the re-append must take the rolled-back targets"
+        if f % 3 == 2:                          # commit the deferred evictions every third frame
+            st.set_defer(False)
+            st.evict()
+            st.set_defer(True)
+        ref.append()
+        ref.evict()
+        if f % 3 == 2:
+            assert st.visible_sources() == ref.visible_sources(), f"frame {f}: deferred != plain eviction"
+            total = len(st.free) + len(st.scale) + len(st.live)
+            assert total == st.num_patch_ids and len(set(st.free) | set(st.scale) | set(st.live)) == total
+    try:
+        st.rollback(); st.rollback()            # one rollback per append
+        raise AssertionError("a second rollback must be refused")
+    except oracle.RollbackUnavailable:
+        pass
+
+
 PINS = {
     "golden_stats": pin_golden_stats,
     "closed_forms": lambda: [pin_closed_forms(c) for c in SMALL_VARIANTS],
@@ -231,6 +269,7 @@ PINS = {
     "permutation": pin_permutation,
     "attention_closed_forms": pin_attention_closed_forms,
     "merge": pin_merge,
+    "rollback": lambda: [pin_rollback(c) for c in SMALL_VARIANTS if c.num_streams == 1],
 }
 
 
@@ -271,6 +310,23 @@ def test_attention_closed_forms():
 
 def test_lse_merge():
     pin_merge()
+
+
+def test_rollback_and_deferred_eviction():
+    for c in SMALL_VARIANTS:
+        if c.num_streams == 1:
+            pin_rollback(c)
+
+
+def test_rollback_needs_the_page_still_held():
+    st = make_streams(_small(scale_frames=0, sliding_window=0, frames=4))[0]
+    st.append()
+    st.evict()                                  # w = 0 and no deferral: the page is already free
+    with pytest.raises(oracle.RollbackUnavailable):
+        st.rollback()
+    st2 = make_streams(_small(frames=4))[0]
+    with pytest.raises(oracle.RollbackUnavailable):
+        st2.rollback()                          # nothing appended
 
 
 def test_append_failure_changes_nothing():
@@ -358,7 +414,34 @@ def _sources_skip_pad_wrong(self):
     return out
 
 
+def _rollback_page_to_back(self):
+    pid, in_scale, opened, targets = self.undo
+    (self.scale if in_scale else self.live).pop()
+    self.free.append(pid)
+    for sp, slot in targets:
+        del self.contents[sp][slot]
+    for sp in reversed(opened):
+        self.special_pages.pop()
+        self.special_free.appendleft(sp)
+    self.special_tokens -= self.S
+    self.frame_count -= 1
+    self.undo = None
+
+
+def _rollback_keeps_special_pages(self):
+    pid, in_scale, opened, targets = self.undo
+    (self.scale if in_scale else self.live).pop()
+    self.free.appendleft(pid)
+    for sp, slot in targets:
+        del self.contents[sp][slot]
+    self.special_tokens -= self.S
+    self.frame_count -= 1
+    self.undo = None
+
+
 MUTATIONS = {
+    "rollback_page_to_back_of_free_list": (opc.StreamPages, "rollback", _rollback_page_to_back),
+    "rollback_keeps_opened_special_pages": (opc.StreamPages, "rollback", _rollback_keeps_special_pages),
     "window_excludes_current_frame": (opc.StreamPages, "evict", _evict_keep_one_less),
     "lifo_eviction": (opc.StreamPages, "evict", _evict_lifo),
     "scale_pages_evicted": (opc.StreamPages, "evict", _evict_scale_too),
@@ -382,6 +465,6 @@ def test_planted_mistake_is_caught(name, monkeypatch):
     for pin_name, pin in PINS.items():
         try:
             pin()
-        except (AssertionError, KeyError, IndexError, ValueError):
+        except (AssertionError, KeyError, IndexError, ValueError, RuntimeError):
             caught.append(pin_name)
     assert caught, f"no pin caught the planted mistake {name}"
