@@ -25,10 +25,10 @@
 //   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
 //               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
 //               every tail row; warp q owns keys [32q, 32q+32) of each chunk and keeps
-//               its own (max, sum, O) per row.  Its P goes to a shared-memory tile in
-//               which the rows of key group q sit in TMEM lane quarter q, so one
-//               O2 += P2 V MMA accumulates the four partial states side by side; they
-//               are merged at the end.
+//               its own (max, sum, O) per row.  Its P goes to rows 16q.. of a 64-row
+//               shared-memory tile; one O2 += P2 V MMA with M = 64 (whose rows
+//               16q..16q+15 live in TMEM lane quarter q) accumulates the four partial
+//               states side by side; they are merged at the end.
 //   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
 //               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
 //               swizzle, into a ring of shared-memory stages.
@@ -57,6 +57,7 @@ namespace spk {
 namespace {
 
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
+constexpr int kP2ColBlockBytes = 64 * 128;  // the tail's 64-row P tile: one column block
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kTailMaxRows = 8;            // rows of the tail (the transposed tail MMA has N = 16)
 constexpr int kTailN = 16;
@@ -74,12 +75,12 @@ struct Cfg {
   // D == 64: the row sums come out of the PV MMA, whose B operand is V extended by a
   // 16-column block of ones (O gets 16 more columns, each holding the row sum)
   static constexpr bool kOnes = (D == 64);
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr int kQ0 = 0;
   static constexpr int kQ1 = kTile;
   static constexpr int kQ2 = 2 * kTile;                 // tail Q: kTailN rows x 128 bytes (D == 64)
-  static constexpr int kP2 = kQ2 + 2048;                // two tail P tiles: 128 rows x 128 keys bf16 each
-  static constexpr int kP2Bytes = 2 * kColBlockBytes;
+  static constexpr int kP2 = kQ2 + 2048;                // two tail P tiles: 64 rows x 128 keys bf16 each
+  static constexpr int kP2Bytes = 2 * kP2ColBlockBytes;
   static constexpr int kKV = kTail ? kP2 + 2 * kP2Bytes : 2 * kTile;
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kOnesBlk = kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones (kOnes)
@@ -98,6 +99,7 @@ struct Cfg {
   static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kOnesBlk % 1024 == 0,
                 "128-byte-swizzled tiles start on 1024-byte boundaries");
   static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
+  static_assert(kTailMaxRows <= 16, "a key group's tail rows fit the 16 rows of its M = 64 quarter");
   static_assert(kLaunch <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -133,10 +135,10 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Byte address of element (row, key) of the tail's P tile: 128 rows x 128 keys bf16,
-// K-major, 128-byte swizzle, keys 0-63 and 64-127 in two 16 KB column blocks.
+// Byte address of element (row, key) of the tail's P tile: 64 rows x 128 keys bf16,
+// K-major, 128-byte swizzle, keys 0-63 and 64-127 in two 8 KB column blocks.
 __device__ __forceinline__ uint32_t p2_addr(uint32_t base, int row, int key) {
-  return base + uint32_t((key >> 6) * kColBlockBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+  return base + uint32_t((key >> 6) * kP2ColBlockBytes + (row >> 3) * 1024 + (row & 7) * 128 +
                          ((((key & 63) >> 3) ^ (row & 7)) << 4) + (key & 7) * 2);
 }
 
@@ -453,9 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // Tail: S2^T = K Q2^T (M = 128 keys, N = 16 tail rows, K = 64), then
-        // O2 (+)= P2 V (M = 128, N = 64, K = 128 keys) with P2 from shared memory.
+        // O2 (+)= P2 V (M = 64, N = 64, K = 128 keys) with P2 from shared memory.  With
+        // M = 64 the accumulator's rows 16q..16q+15 live in TMEM lanes 32q..32q+15, so
+        // P2 row 16q + r (key group q, tail row r) lands in tail warp q's lane r.
         constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailN, 0, 0);
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 64, 0, 1);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(64, 64, 0, 1);
         const uint32_t q2_lo = uint32_t(ptx::smem_desc_sw128(sQ2, 16, 1024));
         const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
         const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_lo = p2_lo + uint32_t((c & 1) * (C::kP2Bytes >> 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+            const uint32_t off = uint32_t((k >> 2) * (kP2ColBlockBytes >> 4) + (k & 3) * 2);
             if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
             else ptx::mma_ss_lh<1>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
           }
@@ -719,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg_m = (m[rr] == -INFINITY) ? 0.f : -m[rr];  // no key seen yet: p = 0
             const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs[rr] + neg_m));
             l[rr] += __bfloat162float(pb);
-            st_shared_u16(p2_addr(sP2 + uint32_t((j & 1) * C::kP2Bytes), 32 * q + rr, key), __bfloat16_as_ushort(pb));
+            st_shared_u16(p2_addr(sP2 + uint32_t((j & 1) * C::kP2Bytes), 16 * q + rr, key), __bfloat16_as_ushort(pb));
           }
         }
         ptx::fence_proxy_async_smem();  // P2 stores -> visible to the tensor core
