@@ -354,6 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the merge kernel that follows may be scheduled now; it waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer

@@ -54,6 +54,9 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
 // 512-byte run; the split loop is unrolled so the loads of several splits are in flight.
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  // launched as a programmatic dependent of the attention kernel: wait until that grid
+  // has completed and its partials are visible (returns at once otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int V = D / 4;  // float4 per row
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = int64_t(p.B) * p.H * V * p.T;
@@ -70,19 +73,27 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   const int64_t lse_step = int64_t(p.H) * p.T;                         // next split, same (head, row)
   const int64_t o0 = part_o_offset<D>(sd.split_base, h, t, 4 * c4, p.H, p.T);
   const int64_t o_step = int64_t(p.H) * D * p.T;
+  // every split's log-sum-exp in flight at once, then the weights
+  float lse[kMaxSplitsPerStream];
+#pragma unroll
+  for (int j = 0; j < kMaxSplitsPerStream; ++j)
+    lse[j] = j < sd.nsplit ? __ldg(&p.part_lse[lse0 + j * lse_step]) : -INFINITY;
   float m = -INFINITY;
-  for (int j = 0; j < sd.nsplit; ++j) m = fmaxf(m, __ldg(&p.part_lse[lse0 + j * lse_step]));
+#pragma unroll
+  for (int j = 0; j < kMaxSplitsPerStream; ++j) m = fmaxf(m, lse[j]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
-#pragma unroll 4
-  for (int j = 0; j < sd.nsplit; ++j) {
-    const float w = exp2f(__ldg(&p.part_lse[lse0 + j * lse_step]) - m);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + o0 + j * o_step));
-    wsum += w;
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+  for (int j = 0; j < kMaxSplitsPerStream; ++j) {
+    if (j < sd.nsplit) {
+      const float w = exp2f(lse[j] - m);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + o0 + j * o_step));
+      wsum += w;
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
   }
   const float inv = 1.f / wsum;
   OutT* out = static_cast<OutT*>(p.out) + ((int64_t(s) * p.T + t) * p.H + h) * D + 4 * c4;
@@ -101,14 +112,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s) {
   const int64_t threads = int64_t(p.B) * p.T * p.H * (p.D / 4);
   const int blocks = int((threads + 255) / 256);
+  // programmatic dependent launch: the merge grid may be scheduled while the attention
+  // kernel still runs (that kernel signals early); its griddepcontrol.wait orders it
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
   if (dtype == 0) {
-    if (p.D == 64) merge_kernel<64, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
-    else merge_kernel<128, __nv_bfloat16><<<blocks, 256, 0, s>>>(p);
-  } else {
-    if (p.D == 64) merge_kernel<64, float><<<blocks, 256, 0, s>>>(p);
-    else merge_kernel<128, float><<<blocks, 256, 0, s>>>(p);
+    if (p.D == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64, __nv_bfloat16>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<128, __nv_bfloat16>, p);
   }
-  return cudaGetLastError();
+  if (p.D == 64) return cudaLaunchKernelEx(&cfg, merge_kernel<64, float>, p);
+  return cudaLaunchKernelEx(&cfg, merge_kernel<128, float>, p);
 }
 
 // ------------------------------------------------------------------ fp32 attention
