@@ -395,34 +395,57 @@ def run_gpu(args, w: wl.Workload):
     launch_ms = [a.elapsed_time(b) for a, b in ev_pairs]
 
     # ------------------------------------------------ e2e: host buffers, copies in the timed region
+    # Every step copies its q/k/v from pinned host memory and its outputs back.  The
+    # copies run on their own streams (host->device, device->host) so block b+1's inputs
+    # move while block b computes; events order each copy against the compute stream.
     hq = [[qcat[vi][b].cpu().pin_memory() for b in range(L)] for vi in range(NV)]
     hkv = [[[tuple(x.cpu().pin_memory() for x in kvs[vi][s][b]) for b in range(L)] for s in range(B)]
            for vi in range(NV)]
-    dq = [torch.empty_like(qcat[0][b]) for b in range(L)]
-    dkv = [[tuple(torch.empty_like(x) for x in kvs[0][s][b]) for b in range(L)] for s in range(B)]
+    dq = [[torch.empty_like(qcat[0][b]) for b in range(L)] for _ in range(2)]          # [set][block]
+    dkv = [[[tuple(torch.empty_like(x) for x in kvs[0][s][b]) for b in range(L)] for s in range(B)]
+           for _ in range(2)]                                                            # [set][stream][block]
     hout = [torch.empty(outs[b].shape, dtype=outs[b].dtype).pin_memory() for b in range(L)]
     h2d = sum(x.numel() * x.element_size() for b in range(L) for x in (hq[0][b],)) + \
         sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b])
     d2h = sum(x.numel() * x.element_size() for x in hout)
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [[torch.cuda.Event() for _ in range(L)] for _ in range(2)]      # inputs of (set, block) landed
+    ev_used = [[None] * L for _ in range(2)]                                # compute done with (set, block)
+    ev_out = [torch.cuda.Event() for _ in range(L)]                         # out[b] written
+    ev_back = [None] * L                                                    # out[b] copied to the host
 
     def e2e_step(f):
-        vi = f % NV
-        for b in range(L):
-            dq[b].copy_(hq[vi][b], non_blocking=True)
-            for s in range(B):
-                dkv[s][b][0].copy_(hkv[vi][s][b][0], non_blocking=True)
-                dkv[s][b][1].copy_(hkv[vi][s][b][1], non_blocking=True)
+        vi, st = f % NV, f % 2
+        with torch.cuda.stream(up):
+            for b in range(L):
+                if ev_used[st][b] is not None:
+                    up.wait_event(ev_used[st][b])
+                dq[st][b].copy_(hq[vi][b], non_blocking=True)
+                for s in range(B):
+                    dkv[st][s][b][0].copy_(hkv[vi][s][b][0], non_blocking=True)
+                    dkv[st][s][b][1].copy_(hkv[vi][s][b][1], non_blocking=True)
+                ev_in[st][b].record(up)
+        stream.wait_event(ev_in[st][0])
         for s in range(B):
-            cache.append_frame(s, 0, dkv[s][0][0], dkv[s][0][1], stream)
+            cache.append_frame(s, 0, dkv[st][s][0][0], dkv[st][s][0][1], stream)
         for s in range(B):
             cache.evict_frames(s)
         cache.plan(ws, stream)
         for b in range(L):
             if b:
+                stream.wait_event(ev_in[st][b])
                 for s in range(B):
-                    cache.append_frame(s, b, dkv[s][b][0], dkv[s][b][1], stream)
-            cache.run_attention(b, dq[b], outs[b], ws, stream)
-            hout[b].copy_(outs[b], non_blocking=True)
+                    cache.append_frame(s, b, dkv[st][s][b][0], dkv[st][s][b][1], stream)
+            if ev_back[b] is not None:
+                stream.wait_event(ev_back[b])       # the previous step's copy of out[b] is done
+            cache.run_attention(b, dq[st][b], outs[b], ws, stream)
+            ev_out[b].record(stream)
+            ev_used[st][b] = ev_out[b]
+            with torch.cuda.stream(down):
+                down.wait_event(ev_out[b])
+                hout[b].copy_(outs[b], non_blocking=True)
+                ev_back[b] = torch.cuda.Event()
+                ev_back[b].record(down)
 
     for _ in range(2):
         e2e_step(f)
@@ -433,9 +456,12 @@ def run_gpu(args, w: wl.Workload):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up.wait_event(e0)
     for _ in range(K):
         e2e_step(f)
         f += 1
+    for b in range(L):
+        stream.wait_event(ev_back[b])              # every output is back on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1000.0, device=dev)
