@@ -190,9 +190,11 @@ int spk_plan_queries(spk_cache* cache, int query_frames, void* workspace, void* 
 
 /* Attention of the current frame for one block, all streams in one launch.
  * q: device [B*T, H, D] (stream s owns rows s*T..s*T+T-1), out: device [B*T, H, D],
- * both in the cache dtype.  workspace must be the one given to spk_plan.  Launches
- * the attention kernel and, when a stream has several KV splits, the merge kernel.
- * Requires a current plan and block's K/V appended for this frame on every stream. */
+ * both in the cache dtype; with spk_plan_queries, T stands for query_frames * T.
+ * workspace must be the one given to the plan.  Launches the attention kernel and,
+ * when a stream has several KV splits, the merge kernel (as a programmatic dependent
+ * launch that waits for the attention grid).  Requires a current plan and block's K/V
+ * appended for this frame on every stream. */
 int spk_run_attention(spk_cache* cache, int block, const void* q, void* out, void* workspace,
                       void* cuda_stream);
 
