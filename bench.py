@@ -115,11 +115,17 @@ KERNEL_SOURCES = ("streaming_paged_kv_two_gb300/csrc/spk_attn_tc.cu", "streaming
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: line comments and blank lines are left out, so
+    editing a comment does not retire the recorded counters."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            for line in fh:
+                code = re.sub(r"//.*$", "", line).strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -13,15 +13,17 @@
 //
 // One CTA (one per SM) = (KV split, head, query-row group).  A group is up to two
 // 128-row "main" tiles, plus, on the last group when head_dim is 64, a "tail" of at
-// most 16 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
+// most 8 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
 //   warps 4-7   softmax of main tile 0, warps 8-11 softmax of main tile 1: one
 //               thread per query row (= TMEM lane).  Each tile has two 64-key score
 //               buffers in TMEM, so Q K^T of the next half chunk runs on the tensor
 //               core while the softmax works on the current one.  fp32 online
-//               softmax in log2 units, masking of the chunk's ragged tail, P written
-//               back as bf16 over S, row sums taken from the rounded P that the MMA
-//               consumes, O rescaled in TMEM only when the running maximum grows by
-//               more than 2^8.
+//               softmax in log2 units: a half's scores are exponentiated against the
+//               running max while their own max is taken, and only when that max
+//               exceeds the running one by more than 2^8 is O rescaled in TMEM and
+//               the half recomputed; masking of the chunk's ragged tail; P written
+//               back as bf16 over S; row sums taken from the rounded P that the MMA
+//               consumes.
 //   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
 //               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
 //               every tail row; warp q owns keys [32q, 32q+32) of each chunk and keeps
