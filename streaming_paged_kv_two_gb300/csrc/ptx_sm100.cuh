@@ -288,6 +288,13 @@ __device__ __forceinline__ float add_bf16x2_to(uint32_t pk, float acc) {
   return d;
 }
 
+// 2^x of a packed pair of bf16 values, result a packed pair of bf16
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

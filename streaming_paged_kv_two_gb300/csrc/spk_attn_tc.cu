@@ -94,6 +94,10 @@ struct Cfg {
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kOW = D + (kOnes ? 16 : 0);  // TMEM columns of a main tile's O
+  // The main softmax moves its running max when a score exceeds it by more than this
+  // (log2 units): 2^8 with fp32 exponentials; 2^2 with paired bf16 ones (D = 64), which
+  // bounds the argument's bf16 rounding.
+  static constexpr float kThreshold = kOnes ? 2.0f : kRescaleThreshold;
   static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + kOW;
   static constexpr uint32_t kO2 = 4 * kHalfKeys + 2 * kOW, kS2 = kO2 + 64;  // D == 64 only: O2, S2^T[2]
   static_assert(kTail ? kS2 + 2 * kTailN <= 512 : kO1 + kOW <= 512, "TMEM budget");
@@ -180,8 +184,14 @@ __device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* 
     const int i = 2 * (e & 15);
     float x0, x1;
     ptx::fma2(x0, x1, __uint_as_float(s[i]), __uint_as_float(s[i + 1]), sl2, neg_m);
-    pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
-    if constexpr (kSum) sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
+    if constexpr (kSum) {
+      pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
+      sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
+    } else {
+      // the row sums come from the MMA: exponentiate the bf16-rounded arguments as a
+      // pair (x <= 2 here, so the argument's rounding moves p by at most 0.27 %)
+      pk[e] = ptx::ex2_bf16x2(pack_bf16(x0, x1));
+    }
   }
   return (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
@@ -592,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mask32(sb, kHalfKeys * b + 32, len);
           const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
           const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk);
-          const bool need = mx > m + kRescaleThreshold;
+          const bool need = mx > m + C::kThreshold;
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? mx : m;
             const float corr = need ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
