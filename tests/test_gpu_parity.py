@@ -191,6 +191,34 @@ def test_tensor_core_scores_match(D):
     h.close()
 
 
+def test_trace_mode_gives_the_same_output_and_ordered_events():
+    """spk_debug_trace_attention: same output as spk_run_attention; CTA 0's recorded
+    clocks are filled for every chunk and ordered along the pipeline."""
+    gh = _h()
+    w = small(frames=6, num_blocks=1)
+    h = gh.Harness(w, splits=2)
+    for f in range(w.frames):
+        h.append(0, 0, *wl.frame_kv(w, 0, 0, f))
+        h.cache.evict_frames(0)
+    h.plan()
+    q = gh.to_device(wl.frame_q(w, 0, 0, w.frames - 1), "bf16")
+    ref = torch.empty_like(q)
+    h.cache.run_attention(0, q, ref, h.ws, h.stream)
+    out = torch.empty_like(q)
+    cap = 64
+    tr = torch.zeros((20, cap), dtype=torch.int64, device="cuda")
+    h.cache.debug_trace_attention(0, q, out, h.ws, tr, cap, h.stream)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    t = tr.cpu().numpy()
+    n = int((t[0] != 0).sum())                 # chunks CTA 0 loaded
+    assert n >= 1
+    tma, s0_seen, p0_arrive, p0_seen = t[0, :n], t[11, :n], t[12, :n], t[3, :n]
+    assert (s0_seen > tma).all() and (p0_arrive >= s0_seen).all() and (p0_seen >= p0_arrive).all()
+    assert h.status() == 0
+    h.close()
+
+
 # ------------------------------------------------------------------ attention parity
 
 CASES = {
