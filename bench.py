@@ -1,6 +1,6 @@
 """Throughput of streaming two-stream paged-KV attention on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload steady_state_10k] [--impl reference]
 
 A step is one frame-step of the whole hot path for one stream set: append of the
 frame's K/V for every block, one evict, one plan, and attention (+ merge) for every
@@ -633,7 +633,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=3, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--workload", default="steady_state_10k", choices=sorted(wl.CONFIGS))
     ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_required_bytes_matches_layout():
-    w = wl.CONFIGS[3]
+    w = wl.CONFIGS["steady_state_10k"]
     cfg, keep = cfg_for(w)
     pool, ws = spk.required_bytes(cfg)
     pages = w.num_streams * (w.max_patch_pages + w.max_special_pages)
@@ -60,7 +60,7 @@ def test_required_bytes_matches_layout():
     (dict(max_special_pages=0), "max pages"),
 ])
 def test_invalid_configs_are_rejected(over, needle):
-    cfg, keep = cfg_for(wl.CONFIGS[2], **over)
+    cfg, keep = cfg_for(wl.CONFIGS["lingbot_like_200"], **over)
     with pytest.raises(spk.SpkError) as e:
         spk.required_bytes(cfg)
     assert e.value.code == spk.SPK_ERR_INVALID_ARG
@@ -68,7 +68,7 @@ def test_invalid_configs_are_rejected(over, needle):
 
 
 def test_bad_page_order_is_rejected():
-    w = wl.CONFIGS[5]
+    w = wl.CONFIGS["batched4_d128"]
     po, so = wl.page_orders(w)
     po = po.copy()
     po[3] = po[4]  # duplicate id
@@ -117,14 +117,14 @@ def _compare_stream_run(w: wl.Workload, frames: int, every: int = 1):
     cache.close()
 
 
-@pytest.mark.parametrize("n", [1, 2, 4, 5])
-def test_bookkeeping_matches_oracle_workloads(n):
-    w = wl.CONFIGS[n]
+@pytest.mark.parametrize("name", ["tiny_stream_f32", "lingbot_like_200", "high_res_999", "batched4_d128"])
+def test_bookkeeping_matches_oracle_workloads(name):
+    w = wl.CONFIGS[name]
     _compare_stream_run(w, w.frames, every=1 if w.frames <= 2000 else 7)
 
 
 def test_bookkeeping_matches_oracle_steady_state():
-    w = wl.CONFIGS[3]
+    w = wl.CONFIGS["steady_state_10k"]
     _compare_stream_run(w, w.frames, every=13)
 
 
@@ -136,7 +136,7 @@ def test_bookkeeping_matches_oracle_steady_state():
     dict(num_streams=3, shuffle_pages=True),
 ])
 def test_bookkeeping_matches_oracle_edge_cases(over):
-    base = wl.CONFIGS[2].replace(frames=150, num_blocks=2, **over)
+    base = wl.CONFIGS["lingbot_like_200"].replace(frames=150, num_blocks=2, **over)
     _compare_stream_run(base, base.frames)
 
 
@@ -156,7 +156,7 @@ def test_golden_stats_through_the_library():
 
 
 def _dry(w=None, **over):
-    w = w or wl.CONFIGS[2].replace(num_blocks=3)
+    w = w or wl.CONFIGS["lingbot_like_200"].replace(num_blocks=3)
     cfg, keep = cfg_for(w, **over)
     return spk.Cache(cfg, None, keep)
 
@@ -220,7 +220,7 @@ def test_plan_needs_a_frame_and_dry_cache_has_no_device_calls():
 
 
 def test_reset_restores_initial_order():
-    w = wl.CONFIGS[5].replace(frames=300)
+    w = wl.CONFIGS["batched4_d128"].replace(frames=300)
     cfg, keep = cfg_for(w)
     c = spk.Cache(cfg, None, keep)
     first = []
@@ -241,7 +241,7 @@ def test_reset_restores_initial_order():
 
 
 def test_split_choice_is_valid():
-    w = wl.CONFIGS[3].replace(frames=2000)
+    w = wl.CONFIGS["steady_state_10k"].replace(frames=2000)
     cfg, keep = cfg_for(w)
     c = spk.Cache(cfg, None, keep)
     for f in range(300):
@@ -266,7 +266,7 @@ def test_split_choice_is_valid():
 def test_plan_queries_tables_and_errors():
     """Scale-phase prefill plan ("Frame Processing Loop", num_frames > 1): the visible
     table is that of spk_plan, the query rows per stream are query_frames * T."""
-    w = wl.CONFIGS[3].replace(frames=64)
+    w = wl.CONFIGS["steady_state_10k"].replace(frames=64)
     cfg, keep = cfg_for(w, max_query_frames=8)
     c = spk.Cache(cfg, None, keep)
     T = w.tokens_per_frame
@@ -308,7 +308,7 @@ def test_plan_queries_tables_and_errors():
 
 
 def test_max_query_frames_sizes_the_workspace():
-    w = wl.CONFIGS[3]
+    w = wl.CONFIGS["steady_state_10k"]
     ws = [spk.required_bytes(cfg_for(w, max_query_frames=q)[0])[1] for q in (0, 1, 8)]
     assert ws[0] == ws[1] < ws[2]
     with pytest.raises(spk.SpkError) as e:
@@ -373,7 +373,7 @@ def _op_sequence_matches_oracle(w: wl.Workload, ops: int, seed: int):
     (dict(num_streams=3, shuffle_pages=True, sliding_window=4, scale_frames=2), 5),
 ])
 def test_rollback_and_deferral_match_oracle(over, seed):
-    w = wl.CONFIGS[2].replace(frames=120, num_blocks=2, **over)
+    w = wl.CONFIGS["lingbot_like_200"].replace(frames=120, num_blocks=2, **over)
     _op_sequence_matches_oracle(w, 600, seed)
 
 

@@ -32,11 +32,11 @@ def _patch_visible_at(w, frame, at):
     return frame < min(at, w.scale_frames) or max(w.scale_frames, at - w.sliding_window) <= frame < at
 
 
-@pytest.mark.parametrize("n", [2, 3, 4, 5])
-def test_fullsize_parity(n):
+@pytest.mark.parametrize("name", ["lingbot_like_200", "steady_state_10k", "high_res_999", "batched4_d128"])
+def test_fullsize_parity(name):
     import gpu_harness as gh
 
-    w = wl.CONFIGS[n]
+    w = wl.CONFIGS[name]
     B, L, P = w.num_streams, w.num_blocks, w.patches_per_frame
     blocks = [0, L - 1]
     checks = sorted({w.frames // 2, w.frames})

@@ -222,8 +222,8 @@ def test_trace_mode_gives_the_same_output_and_ordered_events():
 # ------------------------------------------------------------------ attention parity
 
 CASES = {
-    "tiny_stream_f32": (wl.CONFIGS[1], 0),
-    "tiny_stream_bf16": (wl.CONFIGS[1].replace(dtype="bf16", name="tiny_stream_bf16"), 0),
+    "tiny_stream_f32": (wl.CONFIGS["tiny_stream_f32"], 0),
+    "tiny_stream_bf16": (wl.CONFIGS["tiny_stream_f32"].replace(dtype="bf16", name="tiny_stream_bf16"), 0),
     "t262_d64": (small(), 0),
     "t262_d64_split1": (small(), 1),
     "t262_d64_split5": (small(), 5),

@@ -55,7 +55,7 @@ def test_single_rank_helpers_without_a_process_group():
     import bench
     assert bench.reduce_max(3.5) == 3.5
     assert bench.aggregate_throughput(10, 1, 2.0) == 5.0
-    w = bench.wl.CONFIGS[3]
+    w = bench.wl.CONFIGS["steady_state_10k"]
     flops, byts = bench.block_work(w, 10000)
     # closed forms at the 10,000-frame steady state: N = 72*256 + 60000
     assert bench.visible_tokens(w, 10000) == 78432

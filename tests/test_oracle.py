@@ -284,9 +284,9 @@ def test_closed_forms_small(idx):
     pin_closed_forms(SMALL_VARIANTS[idx])
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
-def test_closed_forms_workloads(n):
-    cfg = wl.CONFIGS[n]
+@pytest.mark.parametrize("name", sorted(wl.CONFIGS))
+def test_closed_forms_workloads(name):
+    cfg = wl.CONFIGS[name]
     # every frame of every workload; the dense source list is checked on a stride
     pin_closed_forms(cfg, check_sources_every=max(1, cfg.frames // 20))
 
@@ -297,7 +297,7 @@ def test_brute_force_history(idx):
 
 
 def test_brute_force_config1_shape():
-    pin_brute_force(wl.CONFIGS[1], 99)
+    pin_brute_force(wl.CONFIGS["tiny_stream_f32"], 99)
 
 
 def test_permutation_invariance():

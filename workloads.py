@@ -9,7 +9,7 @@ streaming inference ("How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D
 Reconstruction", sections "Physical Memory Layout" and "Initializing the Cache
 Manager": 256 patch + 6 special tokens per frame, 16 heads of 64, 8 scale
 frames, a 64-frame window, headroom of 16 pages).  The pages print no activation
-statistics, so values are normal draws with a per-workload scale; config 5 adds
+statistics, so values are normal draws with a per-workload scale; batched4_d128 adds
 a per-(stream, head) scale drawn from U[0.25, 2].
 
 Values are drawn in float32 and, for bf16 workloads, rounded to bfloat16
@@ -63,15 +63,15 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-CONFIGS = {
-    1: Workload("tiny_stream_f32", 1, 1, 4, 64, 16, 16, 2, 2, 4, 12, "f32", 1.0,
-                measured_frames=12),
-    2: Workload("lingbot_like_200", 24, 1, 16, 64, 256, 256, 6, 8, 64, 200, "bf16", 0.5),
-    3: Workload("steady_state_10k", 24, 1, 16, 64, 256, 256, 6, 8, 64, 10000, "bf16", 0.5),
-    4: Workload("high_res_999", 24, 1, 16, 64, 1024, 999, 6, 8, 32, 2000, "bf16", 1.0),
-    5: Workload("batched4_d128", 12, 4, 8, 128, 256, 256, 6, 4, 128, 5000, "bf16", 1.0,
-                per_head_scale=True, shuffle_pages=True),
-}
+CONFIGS = {w.name: w for w in (
+    Workload("tiny_stream_f32", 1, 1, 4, 64, 16, 16, 2, 2, 4, 12, "f32", 1.0,
+             measured_frames=12),
+    Workload("lingbot_like_200", 24, 1, 16, 64, 256, 256, 6, 8, 64, 200, "bf16", 0.5),
+    Workload("steady_state_10k", 24, 1, 16, 64, 256, 256, 6, 8, 64, 10000, "bf16", 0.5),
+    Workload("high_res_999", 24, 1, 16, 64, 1024, 999, 6, 8, 32, 2000, "bf16", 1.0),
+    Workload("batched4_d128", 12, 4, 8, 128, 256, 256, 6, 4, 128, 5000, "bf16", 1.0,
+             per_head_scale=True, shuffle_pages=True),
+)}
 
 
 # ---------------------------------------------------------------- bf16 bits
