@@ -15,6 +15,7 @@ Modules
 ``attention``    gather of the visible K/V into dense arrays and exact softmax
                  attention in float64, plus the log-sum-exp merge of partial
                  results.
+``rope``         the 3-D rotary position embedding of q and k before caching.
 
 Every function cites the passage it follows by page title and section.
 Attention values themselves are pinned by closed forms, invariants and a
@@ -30,3 +31,4 @@ from .paged_cache import (  # noqa: F401
     plan,
 )
 from .attention import attend, gather_visible, merge  # noqa: F401
+from .rope import pair_angles, rotate  # noqa: F401

@@ -13,6 +13,10 @@
   exactly as before its append (and the next append takes the same targets);
   deferred evictions, once committed, give the visible frames of a stream that
   never deferred;
+* rotary embedding: angles and rotated values of a hand-worked token (closed-form
+  cos/sin of angles derived by hand from the RoFormer frequencies), pair norms kept,
+  rotations compose additively in position, scores depend only on the position
+  difference, zero positions and empty sections leave x unchanged;
 * planted mistakes in the oracle are caught by at least one of the pins above.
 """
 from __future__ import annotations
@@ -30,6 +34,7 @@ import torch
 import oracle
 import oracle.attention as oatt
 import oracle.paged_cache as opc
+import oracle.rope as orope
 import workloads as wl
 from oracle_cases import make_streams, step
 
@@ -262,6 +267,50 @@ def pin_rollback(cfg):
         pass
 
 
+def pin_rope_worked_example():
+    """D = 8 (4 pairs), sections (2, 1, 0), theta = 100, token at (t, h, w) = (3, 5, 7).
+
+    By hand: pair 0 is axis t, j = 0, frequency 1 -> angle 3; pair 1 is axis t,
+    j = 1 of 2, frequency 100**(-1/2) = 0.1 -> angle 0.3; pair 2 is axis h, j = 0 ->
+    angle 5; pair 3 lies past the sections -> not turned.
+    """
+    x = np.array([1.0, 0.0, 0.0, 1.0, 2.0, 0.0, 3.0, 4.0]).reshape(1, 1, 8)
+    pos = np.array([[3, 5, 7]])
+    ang = orope.pair_angles(pos, (2, 1, 0), 100.0, 8)
+    np.testing.assert_allclose(ang[0], [3.0, 0.3, 5.0, 0.0], rtol=0, atol=1e-15)
+    want = [math.cos(3.0), math.sin(3.0),          # (1, 0) turned by 3
+            -math.sin(0.3), math.cos(0.3),         # (0, 1) turned by 0.3
+            2 * math.cos(5.0), 2 * math.sin(5.0),  # (2, 0) turned by 5
+            3.0, 4.0]
+    np.testing.assert_allclose(orope.rotate(x, pos, (2, 1, 0), 100.0)[0, 0], want, rtol=0, atol=1e-14)
+
+
+def pin_rope_properties(seed=5):
+    """Rotations: pair norms kept, additive in position, scores relative, identity at 0."""
+    rng = np.random.default_rng(seed)
+    T, H, D = 7, 3, 16
+    sections, theta = (3, 2, 2), 10000.0   # 7 of 8 pairs turned
+    x = rng.standard_normal((T, H, D))
+    p1 = rng.integers(-50, 10000, size=(T, 3))
+    p2 = rng.integers(-50, 50, size=(T, 3))
+    y = orope.rotate(x, p1, sections, theta)
+    np.testing.assert_allclose(np.hypot(y[..., 0::2], y[..., 1::2]), np.hypot(x[..., 0::2], x[..., 1::2]),
+                               rtol=1e-12, atol=0)
+    np.testing.assert_array_equal(y[..., 14:], x[..., 14:])  # the pair past the sections
+    np.testing.assert_allclose(orope.rotate(y, p2, sections, theta), orope.rotate(x, p1 + p2, sections, theta),
+                               rtol=0, atol=1e-9)
+    np.testing.assert_array_equal(orope.rotate(x, np.zeros((T, 3), dtype=np.int64), sections, theta), x)
+    np.testing.assert_array_equal(orope.rotate(x, p1, (0, 0, 0), theta), x)
+    # q_i . k_j depends on the position difference only: shift every position alike
+    q, k = x, rng.standard_normal((T, H, D))
+    pq, pk = p2, rng.integers(-50, 50, size=(T, 3))
+    shift = np.array([[1234, -7, 19]])
+    s0 = np.einsum("ihd,jhd->hij", orope.rotate(q, pq, sections, theta), orope.rotate(k, pk, sections, theta))
+    s1 = np.einsum("ihd,jhd->hij", orope.rotate(q, pq + shift, sections, theta),
+                   orope.rotate(k, pk + shift, sections, theta))
+    np.testing.assert_allclose(s1, s0, rtol=0, atol=1e-9)
+
+
 PINS = {
     "golden_stats": pin_golden_stats,
     "closed_forms": lambda: [pin_closed_forms(c) for c in SMALL_VARIANTS],
@@ -270,6 +319,8 @@ PINS = {
     "attention_closed_forms": pin_attention_closed_forms,
     "merge": pin_merge,
     "rollback": lambda: [pin_rollback(c) for c in SMALL_VARIANTS if c.num_streams == 1],
+    "rope_worked_example": pin_rope_worked_example,
+    "rope_properties": pin_rope_properties,
 }
 
 
@@ -310,6 +361,14 @@ def test_attention_closed_forms():
 
 def test_lse_merge():
     pin_merge()
+
+
+def test_rope_worked_example():
+    pin_rope_worked_example()
+
+
+def test_rope_properties():
+    pin_rope_properties()
 
 
 def test_rollback_and_deferred_eviction():
@@ -439,7 +498,42 @@ def _rollback_keeps_special_pages(self):
     self.undo = None
 
 
+_ORIG_PAIR_ANGLES = orope.pair_angles
+
+
+def _rotate_backwards(x, positions, sections, theta):
+    return _ORIG_ROTATE(x, -np.asarray(positions), sections, theta)
+
+
+def _rotate_half_split(x, positions, sections, theta):
+    # pairs (x[i], x[i + D/2]) instead of adjacent pairs
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[2]
+    perm = np.empty(D, dtype=np.int64)
+    perm[0::2] = np.arange(D // 2)
+    perm[1::2] = np.arange(D // 2) + D // 2
+    out = np.empty_like(x)
+    out[..., perm] = _ORIG_ROTATE(x[..., perm], positions, sections, theta)
+    return out
+
+
+def _angles_full_dim_exponent(positions, sections, theta, head_dim):
+    # theta**(-2j/n) instead of theta**(-j/n)
+    return _ORIG_PAIR_ANGLES(positions, sections, float(theta) ** 2, head_dim)
+
+
+def _angles_axis_swapped(positions, sections, theta, head_dim):
+    return _ORIG_PAIR_ANGLES(np.asarray(positions)[:, [1, 0, 2]], sections, theta, head_dim)
+
+
+_ORIG_ROTATE = orope.rotate
+
+
 MUTATIONS = {
+    "rope_turns_backwards": (orope, "rotate", _rotate_backwards),
+    "rope_half_split_pairs": (orope, "rotate", _rotate_half_split),
+    "rope_frequency_exponent_doubled": (orope, "pair_angles", _angles_full_dim_exponent),
+    "rope_axes_swapped": (orope, "pair_angles", _angles_axis_swapped),
     "rollback_page_to_back_of_free_list": (opc.StreamPages, "rollback", _rollback_page_to_back),
     "rollback_keeps_opened_special_pages": (opc.StreamPages, "rollback", _rollback_keeps_special_pages),
     "window_excludes_current_frame": (opc.StreamPages, "evict", _evict_keep_one_less),

@@ -150,6 +150,40 @@ def frame_q(cfg: Workload, stream: int, block: int, frame: int) -> np.ndarray:
     return _finish(cfg, q, stream)
 
 
+def patch_grid(cfg: Workload):
+    """(rows, cols) of the frame's patch grid: the most nearly square factorisation of P
+    with rows <= cols (16 x 16 for 256 patches, 27 x 37 for 999)."""
+    P = cfg.patches_per_frame
+    rows = int(np.floor(np.sqrt(P)))
+    while P % rows:
+        rows -= 1
+    return rows, P // rows
+
+
+def frame_positions(cfg: Workload, frame: int, frame_offset: int = 0) -> np.ndarray:
+    """Rotary positions (t, h, w) of a frame's T tokens, int32 [T, 3].
+
+    t is the global frame index (frame + frame_offset) for every token; patch p sits
+    at (p // cols, p % cols) of the patch grid; special tokens sit at (-1, -1), off
+    the grid.
+    """
+    rows, cols = patch_grid(cfg)
+    P, T = cfg.patches_per_frame, cfg.tokens_per_frame
+    pos = np.empty((T, 3), dtype=np.int32)
+    pos[:, 0] = frame + frame_offset
+    p = np.arange(P)
+    pos[:P, 1] = p // cols
+    pos[:P, 2] = p % cols
+    pos[P:, 1:] = -1
+    return pos
+
+
+def rope_sections(cfg: Workload):
+    """Rotary pairs per axis (t, h, w): h and w a third of the D/2 pairs each, t the rest."""
+    n = cfg.head_dim // 2
+    return (n - 2 * (n // 3), n // 3, n // 3)
+
+
 def page_orders(cfg: Workload):
     """Initial free-list orders as global page ids, or (None, None) for ascending.
 
