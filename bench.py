@@ -307,7 +307,7 @@ def run_gpu(args, w: wl.Workload):
 
     K, W = args.steps, args.warmup
     total_frames = w.frames
-    extra = W + K + 2                       # the e2e pass streams past the steady-state frame
+    extra = W + K + 4                       # the append-timing and e2e passes stream past the steady-state frame
     wk = w.replace(frames=total_frames + extra)
     cfg, keep = spk_config_for(wk, args.splits)
     pool_bytes, ws_bytes = spk.required_bytes(cfg)
@@ -325,12 +325,34 @@ def run_gpu(args, w: wl.Workload):
            for vi in range(NV)]
     qcat = [[torch.cat([qs[vi][s][b] for s in range(B)]) for b in range(L)] for vi in range(NV)]
     outs = [torch.empty_like(qcat[0][b]) for b in range(L)]
+    # --rope: append through the fused rotary scatter; q is turned into qrot, which attention reads
+    sections, theta = wl.rope_sections(w), 10000.0
+    qrot = [torch.empty_like(qcat[0][b]) for b in range(L)] if args.rope else None
+    pos_all = (torch.from_numpy(np.stack([wl.frame_positions(w, x) for x in range(wk.frames)])).to(dev)
+               if args.rope else None)
+    ev_app = []
 
-    def append_all(f, b):
+    def append_one(f, s, b, k, v, q=None, pos=None):
+        if not args.rope:
+            cache.append_frame(s, b, k, v, stream)
+            return
+        pos = pos_all[f] if pos is None else pos
+        cache.append_frame_rope(s, b, k, v, q if q is not None else qs[f % NV][s][b], qrot[b][s * T:(s + 1) * T],
+                                pos, sections, theta, stream)
+
+    def append_all(f, b, timed=False):
         vi = f % NV
         for s in range(B):
             k, v = kvs[vi][s][b]
-            cache.append_frame(s, b, k, v, stream)
+            if timed:
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                append_one(f, s, b, k, v)
+                a1.record(stream)
+                ev_app.append((a0, a1))
+            else:
+                append_one(f, s, b, k, v)
 
     # fast-forward: frames whose attention is not timed only need their K/V appended
     t_ff = time.perf_counter()
@@ -338,7 +360,7 @@ def run_gpu(args, w: wl.Workload):
     for f in range(pre):
         for s in range(B):
             k, v = kvs[f % NV][s][0]
-            cache.append_frame(s, 0, k, v, stream)
+            append_one(f, s, 0, k, v)
             cache.evict_frames(s)
         for b in range(1, L):
             append_all(f, b)
@@ -347,18 +369,18 @@ def run_gpu(args, w: wl.Workload):
 
     ev_pairs = []
 
-    def frame_step(f, timed_launches=False, q_override=None, out_override=None):
+    def frame_step(f, timed_launches=False, timed_appends=False, q_override=None, out_override=None):
         vi = f % NV
         for s in range(B):
             k, v = kvs[vi][s][0]
-            cache.append_frame(s, 0, k, v, stream)
+            append_one(f, s, 0, k, v)
         for s in range(B):
             cache.evict_frames(s)
         cache.plan(ws, stream)
         for b in range(L):
             if b:
-                append_all(f, b)
-            q = qcat[vi][b] if q_override is None else q_override[b]
+                append_all(f, b, timed=timed_appends)
+            q = (qrot[b] if args.rope else qcat[vi][b]) if q_override is None else q_override[b]
             o = outs[b] if out_override is None else out_override[b]
             if timed_launches:
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -399,6 +421,13 @@ def run_gpu(args, w: wl.Workload):
     max_elapsed = reduce_max(elapsed, device=dev)
     status = spk.read_device_status(ws, stream)
     launch_ms = [a.elapsed_time(b) for a, b in ev_pairs]
+    # appends timed on their own, outside the timed region (events around every append
+    # launch would slow the step they measure)
+    for _ in range(2):
+        frame_step(f, timed_appends=True)
+        f += 1
+    torch.cuda.synchronize()
+    append_ms = [a.elapsed_time(b) for a, b in ev_app]
 
     # ------------------------------------------------ e2e: host buffers, copies in the timed region
     # Every step copies its q/k/v from pinned host memory and its outputs back.  The
@@ -411,8 +440,11 @@ def run_gpu(args, w: wl.Workload):
     dkv = [[[tuple(torch.empty_like(x) for x in kvs[0][s][b]) for b in range(L)] for s in range(B)]
            for _ in range(2)]                                                            # [set][stream][block]
     hout = [torch.empty(outs[b].shape, dtype=outs[b].dtype).pin_memory() for b in range(L)]
+    hpos = pos_all.cpu().pin_memory() if args.rope else None          # [frame, T, 3]
+    dpos = [torch.empty_like(pos_all[0]) for _ in range(2)] if args.rope else None
     h2d = sum(x.numel() * x.element_size() for b in range(L) for x in (hq[0][b],)) + \
-        sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b])
+        sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b]) + \
+        (hpos[0].numel() * hpos[0].element_size() if args.rope else 0)
     d2h = sum(x.numel() * x.element_size() for x in hout)
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [[torch.cuda.Event() for _ in range(L)] for _ in range(2)]      # inputs of (set, block) landed
@@ -423,6 +455,10 @@ def run_gpu(args, w: wl.Workload):
     def e2e_step(f):
         vi, st = f % NV, f % 2
         with torch.cuda.stream(up):
+            if args.rope:
+                if ev_used[st][L - 1] is not None:
+                    up.wait_event(ev_used[st][L - 1])   # the last append that read dpos[st] is done
+                dpos[st].copy_(hpos[f], non_blocking=True)
             for b in range(L):
                 if ev_used[st][b] is not None:
                     up.wait_event(ev_used[st][b])
@@ -433,7 +469,8 @@ def run_gpu(args, w: wl.Workload):
                 ev_in[st][b].record(up)
         stream.wait_event(ev_in[st][0])
         for s in range(B):
-            cache.append_frame(s, 0, dkv[st][s][0][0], dkv[st][s][0][1], stream)
+            append_one(f, s, 0, dkv[st][s][0][0], dkv[st][s][0][1], q=dq[st][0][s * T:(s + 1) * T],
+                       pos=dpos[st] if args.rope else None)
         for s in range(B):
             cache.evict_frames(s)
         cache.plan(ws, stream)
@@ -441,10 +478,11 @@ def run_gpu(args, w: wl.Workload):
             if b:
                 stream.wait_event(ev_in[st][b])
                 for s in range(B):
-                    cache.append_frame(s, b, dkv[st][s][b][0], dkv[st][s][b][1], stream)
+                    append_one(f, s, b, dkv[st][s][b][0], dkv[st][s][b][1], q=dq[st][b][s * T:(s + 1) * T],
+                               pos=dpos[st] if args.rope else None)
             if ev_back[b] is not None:
                 stream.wait_event(ev_back[b])       # the previous step's copy of out[b] is done
-            cache.run_attention(b, dq[st][b], outs[b], ws, stream)
+            cache.run_attention(b, qrot[b] if args.rope else dq[st][b], outs[b], ws, stream)
             ev_out[b].record(stream)
             ev_used[st][b] = ev_out[b]
             with torch.cuda.stream(down):
@@ -487,11 +525,15 @@ def run_gpu(args, w: wl.Workload):
     value = aggregate_throughput(K, world, max_elapsed)
     step_ms = max_elapsed / K * 1000.0
     launches_per_step = B * L + L + (L if info["merge_needed"] else 0)
+    eb = wl.element_bytes(w)
+    # K and V in and out; with the rotary embedding q in and q out as well
+    append_bytes = (6 if args.rope else 4) * T * w.num_heads * w.head_dim * eb
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {**workload_config(w, f_first + K), "timed_frames": [f_first + 1, f_first + K],
+                   **({"rope": {"sections": list(sections), "theta": theta}} if args.rope else {}),
                    "l2": "no flush: visible K/V per block exceeds L2",
                    "parallelism": f"replicas x{world} (independent streams, no data-path collective)"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
@@ -506,6 +548,12 @@ def run_gpu(args, w: wl.Workload):
         "e2e": {"value": aggregate_throughput(K, world, e2e_elapsed), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "frames": [f - K + 1, f]},
+        "append": {"kernel": "append_rope_kernel" if args.rope else "append_kernel",
+                   "avg_launch_us": statistics.mean(append_ms) * 1e3,
+                   "bytes_per_launch": append_bytes,
+                   "gbs": append_bytes / (statistics.mean(append_ms) * 1e-3) / 1e9,
+                   "note": "blocks 1..L-1 of two frames after the timed region, events around each launch "
+                           "(launch overhead included)"},
         "gpu_launches": launches_per_step * K,
         "plan": info,
         "clocks": clk,
@@ -637,6 +685,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="streaming step: append through the fused 3-D rotary scatter (q and k turned)")
     ap.add_argument("--splits", type=int, default=0,
                     help="tuning only: force this many KV splits per stream (0 = the planner's choice)")
     ap.add_argument("--blocks", type=int, default=0,

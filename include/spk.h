@@ -142,6 +142,43 @@ int spk_reset(spk_cache* cache);
 int spk_append_frame(spk_cache* cache, int stream, int block, const void* k, const void* v,
                      void* cuda_stream);
 
+/* 3-D rotary position embedding applied on append ("How LingBot-Map Uses FlashInfer
+ * KV Cache for Streaming 3D Reconstruction", "3D RoPE Position Encoding" and the FAQ
+ * "How is temporal information preserved in the KV cache?": q and k are rotated with
+ * positions that carry the global frame index before k enters the cache, so attention
+ * needs no position lookup).  The pages name the embedding without writing it out;
+ * the rotation taken is RoFormer's (Su et al. 2021) per position axis:
+ *   - the head dimension is D/2 adjacent pairs (x[2i], x[2i+1]);
+ *   - pairs [0, sections[0]) follow axis t, the next sections[1] pairs axis h, the
+ *     next sections[2] pairs axis w; later pairs are not turned;
+ *   - pair j of a section of n pairs turns by position_axis * theta^(-j/n):
+ *     (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a).
+ * V is never rotated. */
+typedef struct {
+  int32_t sections[3];  /* turned pairs per axis t, h, w; each >= 0, sum <= D/2 */
+  int32_t reserved;     /* must be 0 */
+  double theta;         /* frequency base; finite and > 0 */
+} spk_rope;
+
+/* spk_append_frame with the rotary embedding fused into the scatter: one kernel
+ * writes rotate(k) and v into the frame's slots (the same targets, bookkeeping, call
+ * order and errors as spk_append_frame) and rotate(q) into q_out.
+ *   positions: device int32 [T, 3], (t, h, w) of each token row (rows as in k);
+ *              any int32 value, negative included.
+ *   q:         device [T, H, D] in the cache dtype, or NULL (then q_out is NULL too
+ *              and only k is rotated).
+ *   q_out:     device [T, H, D]; either q itself (rotated in place) or a buffer that
+ *              does not overlap it.  k, v, q, q_out are 16-byte aligned.
+ *   rope:      host struct, read during the call only.
+ * Arithmetic: theta^(-j/n) in double on the host; on the device the angle
+ * position * theta^(-j/n) and its reduction modulo 2*pi in double, sin/cos and the
+ * rotation in fp32, one rounding to the cache dtype.  All arguments are checked
+ * before any bookkeeping changes (SPK_ERR_INVALID_ARG).  On a bookkeeping-only cache
+ * every device pointer is NULL and only the bookkeeping runs. */
+int spk_append_frame_rope(spk_cache* cache, int stream, int block, const void* k, const void* v,
+                          const void* q, void* q_out, const int32_t* positions, const spk_rope* rope,
+                          void* cuda_stream);
+
 /* Evict: move the oldest live-window pages to the free list until at most
  * sliding_window remain.  Host only, no data moves.  Marks the plan stale. */
 int spk_evict_frames(spk_cache* cache, int stream);

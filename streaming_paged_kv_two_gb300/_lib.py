@@ -53,6 +53,10 @@ class spk_stats(ctypes.Structure):
         "frame_count", "scale_pages", "live_pages", "free_pages", "special_tokens")]
 
 
+class spk_rope(ctypes.Structure):
+    _fields_ = [("sections", ctypes.c_int32 * 3), ("reserved", ctypes.c_int32), ("theta", ctypes.c_double)]
+
+
 class spk_plan_info(ctypes.Structure):
     _fields_ = [("num_chunks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("merge_needed", ctypes.c_int32), ("visible_tokens", ctypes.c_int64)]
@@ -71,6 +75,7 @@ def _load():
         "spk_destroy_cache": (I32, [P]),
         "spk_reset": (I32, [P]),
         "spk_append_frame": (I32, [P, I32, I32, P, P, P]),
+        "spk_append_frame_rope": (I32, [P, I32, I32, P, P, P, P, P, ctypes.POINTER(spk_rope), P]),
         "spk_evict_frames": (I32, [P, I32]),
         "spk_plan": (I32, [P, P, P]),
         "spk_set_defer_eviction": (I32, [P, I32, I32]),
@@ -193,6 +198,14 @@ class Cache:
 
     def append_frame(self, stream: int, block: int, k=None, v=None, cuda_stream=None):
         _check(lib.spk_append_frame(self._h, stream, block, _ptr(k), _ptr(v), _stream(cuda_stream)))
+
+    def append_frame_rope(self, stream: int, block: int, k=None, v=None, q=None, q_out=None, positions=None,
+                          sections=(0, 0, 0), theta: float = 10000.0, cuda_stream=None):
+        """append_frame with q and k turned by the 3-D rotary embedding (k into the cache,
+        q into q_out, which may be q itself).  positions: device int32 [T, 3]."""
+        rope = spk_rope((ctypes.c_int32 * 3)(*sections), 0, float(theta))
+        _check(lib.spk_append_frame_rope(self._h, stream, block, _ptr(k), _ptr(v), _ptr(q), _ptr(q_out),
+                                         _ptr(positions), ctypes.byref(rope), _stream(cuda_stream)))
 
     def evict_frames(self, stream: int):
         _check(lib.spk_evict_frames(self._h, stream))

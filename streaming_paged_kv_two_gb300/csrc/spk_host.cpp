@@ -484,7 +484,69 @@ int spk_reset(spk_cache* c) {
   return ok();
 }
 
-int spk_append_frame(spk_cache* c, int stream, int block, const void* k, const void* v, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// The rotary part of spk_append_frame_rope, checked and turned into kernel tables.
+struct RopeArgs {
+  const void* q;
+  void* q_out;
+  const int32_t* pos;
+  const spk_rope* rope;
+};
+
+int check_rope(const spk_cache* c, const RopeArgs& ra, AppendRopeParams* rp) {
+  const spk_config& g = c->cfg;
+  const spk_rope* r = ra.rope;
+  if (!r) return fail(SPK_ERR_INVALID_ARG, "rope must point to an spk_rope");
+  if (r->reserved != 0) return fail(SPK_ERR_INVALID_ARG, "spk_rope.reserved must be 0");
+  if (!std::isfinite(r->theta) || !(r->theta > 0.0))
+    return fail(SPK_ERR_INVALID_ARG, "spk_rope.theta must be finite and > 0");
+  int64_t total = 0;
+  for (int a = 0; a < 3; ++a) {
+    if (r->sections[a] < 0) return fail(SPK_ERR_INVALID_ARG, "spk_rope.sections[%d] is negative", a);
+    total += r->sections[a];
+  }
+  if (total > g.head_dim / 2)
+    return fail(SPK_ERR_INVALID_ARG, "spk_rope.sections sum to %lld pairs, head_dim/2 = %d", (long long)total,
+                g.head_dim / 2);
+  if (c->dry) {
+    if (ra.q || ra.q_out || ra.pos)
+      return fail(SPK_ERR_INVALID_ARG, "bookkeeping-only cache takes q = q_out = positions = NULL");
+  } else {
+    if (!ra.pos) return fail(SPK_ERR_INVALID_ARG, "positions must be a device pointer");
+    if ((ra.q == nullptr) != (ra.q_out == nullptr))
+      return fail(SPK_ERR_INVALID_ARG, "q and q_out are both NULL or both device pointers");
+    if ((reinterpret_cast<uintptr_t>(ra.q) | reinterpret_cast<uintptr_t>(ra.q_out)) & 15)
+      return fail(SPK_ERR_INVALID_ARG, "q and q_out must be 16-byte aligned");
+    if (ra.q && ra.q != ra.q_out) {
+      const uintptr_t bytes = uintptr_t(c->T) * g.num_heads * g.head_dim * elem_bytes(g.dtype);
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(ra.q), b0 = reinterpret_cast<uintptr_t>(ra.q_out);
+      if (a0 < b0 + bytes && b0 < a0 + bytes)
+        return fail(SPK_ERR_INVALID_ARG, "q_out overlaps q without being q");
+    }
+  }
+  if (rp) {
+    rp->q = static_cast<const char*>(ra.q);
+    rp->q_out = static_cast<char*>(ra.q_out);
+    rp->pos = ra.pos;
+    rp->head_dim = g.head_dim;
+    rp->rot_pairs = int32_t(total);
+    int i = 0;
+    for (int a = 0; a < 3; ++a) {
+      const int n = r->sections[a];
+      for (int j = 0; j < n; ++j, ++i) {
+        rp->axis[i] = int8_t(a);
+        rp->inv_freq[i] = std::pow(r->theta, -double(j) / double(n));
+      }
+    }
+  }
+  return SPK_OK;
+}
+
+int append_impl(spk_cache* c, int stream, int block, const void* k, const void* v, const RopeArgs* ra,
+                void* cuda_stream) {
   int rc = check_cache(c);
   if (rc) return rc;
   if ((rc = check_stream(c, stream))) return rc;
@@ -497,6 +559,8 @@ int spk_append_frame(spk_cache* c, int stream, int block, const void* k, const v
   } else if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) {
     return fail(SPK_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
   }
+  AppendRopeParams rp{};
+  if (ra && (rc = check_rope(c, *ra, &rp))) return rc;
   StreamState& s = c->st[stream];
   if (block == 0) {
     if ((rc = allocate_frame(c, s))) return rc;
@@ -522,9 +586,29 @@ int spk_append_frame(spk_cache* c, int stream, int block, const void* k, const v
     p.special_page[j] = s.cur_spage[j];
     p.special_slot[j] = s.cur_sslot[j];
   }
-  cudaError_t err = launch_append(p, e, static_cast<cudaStream_t>(cuda_stream));
+  cudaError_t err;
+  if (ra) {
+    rp.a = p;
+    err = launch_append_rope(rp, e, static_cast<cudaStream_t>(cuda_stream));
+  } else {
+    err = launch_append(p, e, static_cast<cudaStream_t>(cuda_stream));
+  }
   if (err != cudaSuccess) return cuda_fail(err, "append kernel launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int spk_append_frame(spk_cache* c, int stream, int block, const void* k, const void* v, void* cuda_stream) {
+  return append_impl(c, stream, block, k, v, nullptr, cuda_stream);
+}
+
+int spk_append_frame_rope(spk_cache* c, int stream, int block, const void* k, const void* v, const void* q,
+                          void* q_out, const int32_t* positions, const spk_rope* rope, void* cuda_stream) {
+  const RopeArgs ra{q, q_out, positions, rope};
+  return append_impl(c, stream, block, k, v, &ra, cuda_stream);
 }
 
 int spk_evict_frames(spk_cache* c, int stream) {

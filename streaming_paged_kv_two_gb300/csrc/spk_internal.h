@@ -80,6 +80,20 @@ struct AppendParams {
   int32_t special_slot[kMaxSpecials];
 };
 
+// Rotary embedding fused into the append: per turned pair its position axis and
+// theta^(-j/n) (double, from the host); kMaxRopePairs covers D <= 128.
+constexpr int kMaxRopePairs = 64;
+struct AppendRopeParams {
+  AppendParams a;
+  const char* q;              // [T, H, D] or nullptr
+  char* q_out;                // [T, H, D] (may be q)
+  const int32_t* pos;         // [T, 3]
+  int32_t head_dim;
+  int32_t rot_pairs;          // pairs turned (sections' sum)
+  double inv_freq[kMaxRopePairs];
+  int8_t axis[kMaxRopePairs];
+};
+
 struct AttnParams {
   const void* pool;
   const void* q;              // [B*T, H, D]
@@ -125,6 +139,7 @@ struct MergeParams {
 
 // Kernel launchers (defined in the .cu files).  All return the launch error.
 cudaError_t launch_append(const AppendParams& p, int elem_bytes, cudaStream_t s);
+cudaError_t launch_append_rope(const AppendRopeParams& p, int elem_bytes, cudaStream_t s);
 cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s);
 cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);

@@ -398,3 +398,61 @@ def test_rollback_restores_block_marks_and_targets():
     with pytest.raises(spk.SpkError) as e:
         c.rollback_frame(0)
     assert e.value.code == spk.SPK_ERR_BAD_STATE
+
+
+# ---------------------------------------------------------------- rotary append (host checks)
+
+def _rope_call(cache, sections=(4, 2, 2), theta=10000.0, reserved=0, stream=0, block=0, **ptrs):
+    rope = spk._lib.spk_rope((ctypes.c_int32 * 3)(*sections), reserved, theta)
+    return spk.lib.spk_append_frame_rope(cache._h, stream, block, ptrs.get("k"), ptrs.get("v"), ptrs.get("q"),
+                                         ptrs.get("q_out"), ptrs.get("positions"), ctypes.byref(rope), None)
+
+
+@pytest.mark.parametrize("bad,needle", [
+    (dict(sections=(-1, 2, 2)), "negative"),
+    (dict(sections=(20, 10, 3)), "head_dim/2"),
+    (dict(theta=0.0), "theta"),
+    (dict(theta=float("nan")), "theta"),
+    (dict(theta=float("inf")), "theta"),
+    (dict(reserved=1), "reserved"),
+    (dict(q=4096), "NULL"),
+    (dict(positions=4096), "NULL"),
+])
+def test_rope_append_rejects_bad_arguments_and_changes_nothing(bad, needle):
+    w = wl.CONFIGS["lingbot_like_200"]          # D = 64: 32 pairs
+    cfg, keep = cfg_for(w)
+    cache = spk.Cache(cfg, None, keep)
+    cache.append_frame_rope(0, 0, sections=(12, 10, 10))
+    cache.append_frame_rope(0, 1, sections=(12, 10, 10))
+    before = (cache.get_stats(0), cache.get_frame_targets(0))
+    rc = _rope_call(cache, **bad)
+    assert rc == spk.SPK_ERR_INVALID_ARG
+    assert needle in spk.last_error()
+    assert (cache.get_stats(0), cache.get_frame_targets(0)) == before
+    with pytest.raises(spk.SpkError):
+        cache.append_frame_rope(0, 0, sections=(-1, 0, 0))
+    assert (cache.get_stats(0), cache.get_frame_targets(0)) == before
+    cache.close()
+
+
+def test_rope_append_keeps_the_bookkeeping_of_append():
+    w = wl.CONFIGS["high_res_999"]
+    cfg, keep = cfg_for(w)
+    a = spk.Cache(cfg, None, keep)
+    b = spk.Cache(cfg, None, keep)
+    for f in range(120):
+        for blk in range(3):
+            a.append_frame(0, blk)
+            b.append_frame_rope(0, blk, sections=wl.rope_sections(w), theta=500.0)
+        assert a.get_frame_targets(0) == b.get_frame_targets(0)
+        a.evict_frames(0)
+        b.evict_frames(0)
+        assert a.get_stats(0) == b.get_stats(0)
+    a.plan()
+    b.plan()
+    assert a.get_plan_host() == b.get_plan_host()
+    with pytest.raises(spk.SpkError) as e:
+        b.append_frame_rope(0, 1, sections=(0, 0, 0))   # block 1 twice in one frame
+    assert e.value.code == spk.SPK_ERR_BAD_STATE
+    a.close()
+    b.close()

@@ -385,3 +385,122 @@ def test_run_attention_state_errors():
     torch.cuda.synchronize()
     assert h.status() == 0
     h.close()
+
+
+# ------------------------------------------------------------------ rotary append
+
+def _rotated_close(got: np.ndarray, want: np.ndarray, x: np.ndarray, dtype: str, what: str):
+    """got (device result, f64) against the fp64 rotation want of x.
+
+    The kernel's fp32 angle reduction, sin/cos and rotation stay within 2e-6 of the
+    pair's norm; bf16 then adds at most half an ulp of the stored value.  fp32 stores
+    keep that 2e-6 bound alone.
+    """
+    norm = np.repeat(np.hypot(x[..., 0::2], x[..., 1::2]), 2, axis=-1)
+    slack = 2e-6 * norm + 1e-30
+    if dtype == "bf16":
+        mag = np.abs(want) + slack
+        half_ulp = np.exp2(np.floor(np.log2(np.maximum(mag, 1e-38))) - 8)
+        bound = half_ulp + slack
+        exact = wl.bf16_bits_to_f64(wl.f32_to_bf16_bits(want.astype(np.float32)))
+        assert np.mean(got == exact) > 0.99, f"{what}: {np.mean(got != exact):.4f} not nearest"
+    else:
+        bound = slack
+    err = np.abs(got - want)
+    assert (err <= bound).all(), f"{what}: worst excess {np.max(err - bound):.3e}"
+
+
+def _rope_fetcher(w, block, sections, theta, offset, cache):
+    base = frame_fetcher(w, 0, block, cache)
+
+    def fetch(frame, rows):
+        k, v = base(frame, rows)
+        pos = wl.frame_positions(w, frame, offset)[np.asarray(rows)]
+        return oracle.rotate(k, pos, sections, theta), v
+    return fetch
+
+
+ROPE_APPEND_CASES = {
+    "bf16_d64_late_frames": (small(frames=5, num_heads=4), (12, 10, 10), 10000.0, 9990),
+    "bf16_d128_pad_straddle": (small(frames=4, head_dim=128, patches_per_frame=200, specials_per_frame=57,
+                                     scale_frames=1, sliding_window=2), (22, 21, 21), 10000.0, 123456),
+    "f32_d128_partial_sections": (small(frames=4, dtype="f32", head_dim=128), (8, 4, 4), 100.0, 0),
+    "bf16_d64_no_sections": (small(frames=3), (0, 0, 0), 10000.0, 7),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROPE_APPEND_CASES))
+def test_rope_append_rotates_k_and_q(name):
+    w, sections, theta, offset = ROPE_APPEND_CASES[name]
+    gh = _h()
+    h = gh.Harness(w)
+    P, rot = w.patches_per_frame, 2 * sum(sections)
+    for f in range(w.frames):
+        pos = wl.frame_positions(w, f, offset)
+        posd = torch.from_numpy(pos).cuda()
+        for b in range(w.num_blocks):
+            k, v = wl.frame_kv(w, 0, b, f)
+            q = wl.frame_q(w, 0, b, f)
+            kd, vd, qd = (gh.to_device(x, w.dtype) for x in (k, v, q))
+            q_out = torch.empty_like(qd) if b == 0 else qd      # block 1 rotates q in place
+            h.cache.append_frame_rope(0, b, kd, vd, qd, q_out, posd, sections, theta, h.stream)
+            torch.cuda.synchronize()
+            pid, targets = h.cache.get_frame_targets(0)
+            page = h.read_page(b, pid)
+            sk = np.concatenate([page[0, :P]] + [h.read_page(b, sp)[0, slot][None] for sp, slot in targets])
+            sv = np.concatenate([page[1, :P]] + [h.read_page(b, sp)[1, slot][None] for sp, slot in targets])
+            assert np.array_equal(sv, v), "V is stored unchanged"
+            # pairs past the sections are copied bit for bit
+            assert np.array_equal(sk[..., rot:], k[..., rot:])
+            got_q = gh.to_f64(q_out)
+            for got, x, label in ((wl.to_f64(sk, w.dtype), wl.to_f64(k, w.dtype), "k"),
+                                  (got_q, wl.to_f64(q, w.dtype), "q")):
+                want = oracle.rotate(x, pos, sections, theta)
+                if rot == 0:
+                    assert np.array_equal(got, x), label
+                else:
+                    _rotated_close(got, want, x, w.dtype, f"{name} frame {f} block {b} {label}")
+        h.cache.evict_frames(0)
+    assert h.status() == 0
+    h.close()
+
+
+@pytest.mark.parametrize("w,offset", [
+    (small(frames=6, num_heads=4), 2000),
+    (small(frames=5, head_dim=128, patches_per_frame=200, specials_per_frame=57, scale_frames=1,
+           sliding_window=2), 0),
+], ids=["bf16_d64", "bf16_d128_pad_straddle"])
+def test_rope_stream_attention_parity(w, offset):
+    """Append with the rotary embedding, attend with the rotated queries: the oracle's
+    attention over its own fp64 rotations of q and of every visible key."""
+    gh = _h()
+    h = gh.Harness(w)
+    streams = make_streams(w)
+    sections, theta = wl.rope_sections(w), 10000.0
+    fetch_cache = {}
+    for f in range(w.frames):
+        pos = wl.frame_positions(w, f, offset)
+        posd = torch.from_numpy(pos).cuda()
+        hold = []
+        for b in range(w.num_blocks):
+            k, v = wl.frame_kv(w, 0, b, f)
+            q = wl.frame_q(w, 0, b, f)
+            kd, vd, qd = (gh.to_device(x, w.dtype) for x in (k, v, q))
+            hold.append((kd, vd, qd))
+            if b == 0:
+                h.cache.append_frame_rope(0, 0, kd, vd, qd, qd, posd, sections, theta, h.stream)
+                streams[0].append()
+                h.cache.evict_frames(0)
+                streams[0].evict()
+                h.plan()
+            else:
+                h.cache.append_frame_rope(0, b, kd, vd, qd, qd, posd, sections, theta, h.stream)
+            out = torch.empty_like(qd)
+            h.cache.run_attention(b, qd, out, h.ws, h.stream)
+            torch.cuda.synchronize()
+            fetch = _rope_fetcher(w, b, sections, theta, offset, fetch_cache.setdefault(b, {}))
+            rq = oracle.rotate(wl.to_f64(q, w.dtype), pos, sections, theta)
+            want = oracle.attend(rq, *oracle.gather_visible(streams[0].visible_sources(), fetch))[0]
+            gh.check_close(gh.to_f64(out), want, w.dtype, f"rope frame {f} block {b}")
+    assert h.status() == 0
+    h.close()
