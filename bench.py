@@ -442,6 +442,7 @@ def run_gpu(args, w: wl.Workload):
     hout = [torch.empty(outs[b].shape, dtype=outs[b].dtype).pin_memory() for b in range(L)]
     hpos = pos_all.cpu().pin_memory() if args.rope else None          # [frame, T, 3]
     dpos = [torch.empty_like(pos_all[0]) for _ in range(2)] if args.rope else None
+    ev_pos = [None, None]                   # the last append that read dpos[set] is done
     h2d = sum(x.numel() * x.element_size() for b in range(L) for x in (hq[0][b],)) + \
         sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b]) + \
         (hpos[0].numel() * hpos[0].element_size() if args.rope else 0)
@@ -456,8 +457,8 @@ def run_gpu(args, w: wl.Workload):
         vi, st = f % NV, f % 2
         with torch.cuda.stream(up):
             if args.rope:
-                if ev_used[st][L - 1] is not None:
-                    up.wait_event(ev_used[st][L - 1])   # the last append that read dpos[st] is done
+                if ev_pos[st] is not None:
+                    up.wait_event(ev_pos[st])
                 dpos[st].copy_(hpos[f], non_blocking=True)
             for b in range(L):
                 if ev_used[st][b] is not None:
@@ -482,6 +483,9 @@ def run_gpu(args, w: wl.Workload):
                                pos=dpos[st] if args.rope else None)
             if ev_back[b] is not None:
                 stream.wait_event(ev_back[b])       # the previous step's copy of out[b] is done
+            if args.rope and b == L - 1:
+                ev_pos[st] = torch.cuda.Event()
+                ev_pos[st].record(stream)
             cache.run_attention(b, qrot[b] if args.rope else dq[st][b], outs[b], ws, stream)
             ev_out[b].record(stream)
             ev_used[st][b] = ev_out[b]

@@ -46,92 +46,6 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ append + rotary
-// The same scatter with the 3-D rotary embedding of q and k fused in ("How LingBot-Map
-// Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "3D RoPE Position
-// Encoding": q and k are rotated before k enters the cache).  One CTA per token row:
-// its threads first turn the row's positions into (cos, sin) per turned pair in shared
-// memory, then move the row's K, V and Q in 16-byte units, rotating the K and Q units
-// that hold turned pairs.  The angle and its reduction modulo 2*pi are taken in double
-// (positions up to 2^31 times frequencies up to 1 keep their fraction of a turn), the
-// sine, cosine and rotation in fp32.
-constexpr double kTwoPiHi = 6.283185307179586;       // 2*pi rounded to double
-constexpr double kTwoPiLo = 2.4492935982947064e-16;  // 2*pi - kTwoPiHi
-constexpr double kInvTwoPi = 0.15915494309189535;
-
-template <typename E>
-__device__ __forceinline__ float elem_to_float(E x);
-template <>
-__device__ __forceinline__ float elem_to_float<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ float elem_to_float<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-template <typename E>
-__device__ __forceinline__ E float_to_elem(float x);
-template <>
-__device__ __forceinline__ float float_to_elem<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 float_to_elem<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
-
-template <typename E>
-__global__ void __launch_bounds__(256) append_rope_kernel(const AppendRopeParams p) {
-  constexpr int kPer = 16 / int(sizeof(E));  // elements per 16-byte unit (even)
-  __shared__ float2 cs[kMaxRopePairs];       // (cos, sin) per turned pair of this row
-  const AppendParams& a = p.a;
-  const int32_t r = blockIdx.x;
-  for (int i = threadIdx.x; i < p.rot_pairs; i += blockDim.x) {
-    const double ang = double(p.pos[3 * r + p.axis[i]]) * p.inv_freq[i];
-    const double n = rint(ang * kInvTwoPi);
-    const double red = fma(-n, kTwoPiLo, fma(-n, kTwoPiHi, ang));
-    float s, c;
-    sincosf(float(red), &s, &c);
-    cs[i] = make_float2(c, s);
-  }
-  __syncthreads();
-  int32_t page, slot;
-  if (r < a.P) {
-    page = a.patch_page;
-    slot = r;
-  } else {
-    page = a.special_page[r - a.P];
-    slot = a.special_slot[r - a.P];
-  }
-  char* kdst = a.pool + int64_t(page) * a.page_bytes + int64_t(slot) * a.row_bytes;
-  const int64_t row_off = int64_t(r) * a.row_bytes;
-  const int32_t upr = int32_t(a.row_bytes >> 4);
-  const int32_t per_head = p.head_dim / kPer;  // units per head
-  const int32_t units = (p.q ? 3 : 2) * upr;
-  for (int32_t u = threadIdx.x; u < units; u += blockDim.x) {
-    const int32_t t = u / upr;  // 0 k, 1 v, 2 q
-    const int32_t c = u - t * upr;
-    const char* src = (t == 0 ? a.k : t == 1 ? a.v : p.q) + row_off + int64_t(c) * 16;
-    char* dst = (t == 0 ? kdst : t == 1 ? kdst + a.half_bytes : p.q_out + row_off) + int64_t(c) * 16;
-    // q may be rotated in place: a plain load (this thread alone reads and writes the unit)
-    uint4 x = t == 2 ? *reinterpret_cast<const uint4*>(src) : __ldg(reinterpret_cast<const uint4*>(src));
-    const int32_t pair0 = (c % per_head) * (kPer / 2);
-    if (t != 1 && pair0 < p.rot_pairs) {
-      E* e = reinterpret_cast<E*>(&x);
-#pragma unroll
-      for (int j = 0; j < kPer / 2; ++j) {
-        if (pair0 + j < p.rot_pairs) {
-          const float2 w = cs[pair0 + j];
-          const float x0 = elem_to_float(e[2 * j]), x1 = elem_to_float(e[2 * j + 1]);
-          e[2 * j] = float_to_elem<E>(fmaf(x0, w.x, -x1 * w.y));
-          e[2 * j + 1] = float_to_elem<E>(fmaf(x0, w.y, x1 * w.x));
-        }
-      }
-    }
-    *reinterpret_cast<uint4*>(dst) = x;
-  }
-}
-
-cudaError_t launch_append_rope(const AppendRopeParams& p, int elem_bytes, cudaStream_t s) {
-  if (elem_bytes == 2)
-    append_rope_kernel<__nv_bfloat16><<<p.a.T, 256, 0, s>>>(p);
-  else
-    append_rope_kernel<float><<<p.a.T, 256, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ merge
 // Exact recombination of softmax attention over disjoint key sets: with
 // M = max_j lse_j (log2 units) and w_j = 2^(lse_j - M),
