@@ -20,10 +20,11 @@
 //               core while the softmax works on the current one.  fp32 online
 //               softmax in log2 units: a half's scores are exponentiated against the
 //               running max while their own max is taken, and only when that max
-//               exceeds the running one by more than 2^8 is O rescaled in TMEM and
-//               the half recomputed; masking of the chunk's ragged tail; P written
-//               back as bf16 over S; row sums taken from the rounded P that the MMA
-//               consumes.
+//               exceeds the running one by more than a threshold (2 for D = 64, whose
+//               exponentials are taken on bf16-rounded argument pairs, 2^8 for
+//               D = 128) is O rescaled in TMEM and the half recomputed; masking of
+//               the chunk's ragged tail; P written back as bf16 over S; row sums
+//               taken from the rounded P that the MMA consumes.
 //   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
 //               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
 //               every tail row; warp q owns keys [32q, 32q+32) of each chunk and keeps
