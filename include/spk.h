@@ -163,8 +163,8 @@ typedef struct {
 /* spk_append_frame with the rotary embedding fused into the scatter: one kernel
  * writes rotate(k) and v into the frame's slots (the same targets, bookkeeping, call
  * order and errors as spk_append_frame) and rotate(q) into q_out.
- *   positions: device int32 [T, 3], (t, h, w) of each token row (rows as in k);
- *              any int32 value, negative included.
+ *   positions: device int32 [T, 3], 4-byte aligned, (t, h, w) of each token row
+ *              (rows as in k); any int32 value, negative included.
  *   q:         device [T, H, D] in the cache dtype, or NULL (then q_out is NULL too
  *              and only k is rotated).
  *   q_out:     device [T, H, D]; either q itself (rotated in place) or a buffer that

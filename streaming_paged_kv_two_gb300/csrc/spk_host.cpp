@@ -515,7 +515,8 @@ int check_rope(const spk_cache* c, const RopeArgs& ra, AppendRopeParams* rp) {
     if (ra.q || ra.q_out || ra.pos)
       return fail(SPK_ERR_INVALID_ARG, "bookkeeping-only cache takes q = q_out = positions = NULL");
   } else {
-    if (!ra.pos) return fail(SPK_ERR_INVALID_ARG, "positions must be a device pointer");
+    if (!ra.pos || (reinterpret_cast<uintptr_t>(ra.pos) & 3))
+      return fail(SPK_ERR_INVALID_ARG, "positions must be a 4-byte aligned device pointer");
     if ((ra.q == nullptr) != (ra.q_out == nullptr))
       return fail(SPK_ERR_INVALID_ARG, "q and q_out are both NULL or both device pointers");
     if ((reinterpret_cast<uintptr_t>(ra.q) | reinterpret_cast<uintptr_t>(ra.q_out)) & 15)

@@ -465,6 +465,36 @@ def test_rope_append_rotates_k_and_q(name):
     h.close()
 
 
+def test_rope_append_argument_errors_launch_nothing():
+    """Misaligned or missing device pointers are refused on the host (SPK_ERR_INVALID_ARG)
+    before any bookkeeping changes or any kernel runs."""
+    import streaming_paged_kv_two_gb300 as spk
+    w = small(frames=2)
+    gh = _h()
+    h = gh.Harness(w)
+    k, v = wl.frame_kv(w, 0, 0, 0)
+    q = wl.frame_q(w, 0, 0, 0)
+    kd, vd, qd = (gh.to_device(x, w.dtype) for x in (k, v, q))
+    posd = torch.from_numpy(wl.frame_positions(w, 0)).cuda()
+    sections = wl.rope_sections(w)
+    before = h.cache.get_stats(0)
+    bad = [dict(positions=posd.data_ptr() + 2), dict(positions=None), dict(q_out=None),
+           dict(q=qd.data_ptr() + 8, q_out=qd.data_ptr() + 8)]
+    for b in bad:
+        args = dict(k=kd, v=vd, q=qd, q_out=qd, positions=posd)
+        args.update(b)
+        with pytest.raises(spk.SpkError) as e:
+            h.cache.append_frame_rope(0, 0, args["k"], args["v"], args["q"], args["q_out"], args["positions"],
+                                      sections, 10000.0, h.stream)
+        assert e.value.code == spk.SPK_ERR_INVALID_ARG
+        assert h.cache.get_stats(0) == before
+    h.cache.append_frame_rope(0, 0, kd, vd, qd, qd, posd, sections, 10000.0, h.stream)
+    torch.cuda.synchronize()
+    assert h.cache.get_stats(0)["frame_count"] == before["frame_count"] + 1
+    assert h.status() == 0
+    h.close()
+
+
 @pytest.mark.parametrize("w,offset", [
     (small(frames=6, num_heads=4), 2000),
     (small(frames=5, head_dim=128, patches_per_frame=200, specials_per_frame=57, scale_frames=1,
