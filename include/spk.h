@@ -58,7 +58,7 @@ enum spk_status {
   SPK_OK = 0,
   SPK_ERR_INVALID_ARG = 1,          /* bad pointer, size, id or configuration */
   SPK_ERR_OUT_OF_PATCH_PAGES = 2,   /* no free patch page for a new frame */
-  SPK_ERR_OUT_OF_SPECIAL_PAGES = 3, /* special pool exhausted ("appends tokens until the pool is exhausted") */
+  SPK_ERR_OUT_OF_SPECIAL_PAGES = 3, /* every special page is full: the special stream only grows */
   SPK_ERR_BAD_STATE = 4,            /* wrong call order: block order, stale or missing plan */
   SPK_ERR_CUDA = 5,                 /* a CUDA runtime/driver call failed */
   SPK_ERR_DEVICE_TIMEOUT = 6        /* a device-side wait ran past its limit; see spk_read_device_status */

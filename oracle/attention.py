@@ -5,9 +5,10 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 Sources (page title, section):
 
 * "How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction",
-  "Attention Kernel Execution": for accuracy checks the manager gathers the
-  visible K/V into dense tensors and runs scaled dot-product attention.  This
-  module is that definition in float64: gather, then for every head
+  "Attention Kernel Execution": the accuracy-check path copies every visible key
+  and value out of the pages into contiguous arrays and applies plain scaled
+  dot-product attention to them.  This module is that definition in float64:
+  gather, then for every head
   softmax(Q K^T / sqrt(D)) V, non-causal, over all visible keys including the
   current frame's own.
 * "How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction",

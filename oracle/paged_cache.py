@@ -9,9 +9,9 @@ Sources (page title, section):
   scale_frames frames kept for good, the next sliding_window frames form the
   recyclable live window; special pages max_patch_pages..max_num_pages-1 are
   append-only and never evicted.
-* same page, "Page Table Planning and Reuse": the visible page table is ordered
-  scale -> window -> specials and paged_kv_last_page_len gives the valid tokens
-  of the final, partially filled page.
+* same page, "Page Table Planning and Reuse": the planned table lists the scale
+  pages first, then the live-window pages, then the special pages, and
+  paged_kv_last_page_len counts the tokens held by the last (possibly partial) page.
 * "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback in
   Streaming Inference", "Two-Stream Design": one frame per patch page; special
   tokens pack contiguously across special pages, a new page taken from the free
