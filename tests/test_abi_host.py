@@ -456,3 +456,19 @@ def test_rope_append_keeps_the_bookkeeping_of_append():
     assert e.value.code == spk.SPK_ERR_BAD_STATE
     a.close()
     b.close()
+
+
+def test_package_refuses_to_import_without_the_library(tmp_path):
+    """No CPU fallback: a copy of the binding without libspk.so fails at import."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "streaming_paged_kv_two_gb300")
+    dst = tmp_path / "streaming_paged_kv_two_gb300"
+    dst.mkdir()
+    for f in ("__init__.py", "_lib.py"):
+        shutil.copy(os.path.join(pkg, f), dst / f)
+    r = subprocess.run([sys.executable, "-c", "import streaming_paged_kv_two_gb300"], cwd=tmp_path,
+                       env={**os.environ, "PYTHONPATH": str(tmp_path)}, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libspk.so is not built" in r.stderr
