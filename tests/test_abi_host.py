@@ -155,6 +155,30 @@ def test_golden_stats_through_the_library():
     assert cache.get_stats(0) == g["expected"]
 
 
+def test_visible_page_order_through_the_library():
+    """The library's plan against the hand-worked page tables of the golden fixture (scale -> window
+    oldest first -> specials in opening order, streams in index order)."""
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "visible_page_order.json")))
+    for case in ("single_stream", "two_streams"):
+        s = g[case]["setup"]
+        cfg, keep = spk.make_config(num_blocks=1, num_streams=s["num_streams"], num_heads=2, head_dim=64,
+                                    page_size=s["page_size"], patches_per_frame=s["patches_per_frame"],
+                                    specials_per_frame=s["specials_per_frame"], scale_frames=s["scale_frames"],
+                                    sliding_window=s["sliding_window"], max_patch_pages=s["max_patch_pages"],
+                                    max_special_pages=s["max_special_pages"])
+        cache = spk.Cache(cfg, None, keep)
+        for want in g[case]["after_frame"]:
+            for b in range(s["num_streams"]):
+                cache.append_frame(b, 0)
+            for b in range(s["num_streams"]):
+                cache.evict_frames(b)
+            cache.plan()
+            got = cache.get_plan_host()
+            want = {k: v for k, v in want.items() if k != "frame"}
+            assert got == want, (case, got, want)
+
+
 def _dry(w=None, **over):
     w = w or wl.CONFIGS["lingbot_like_200"].replace(num_blocks=3)
     cfg, keep = cfg_for(w, **over)

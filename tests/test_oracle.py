@@ -1,6 +1,9 @@
 """Pins of the fp64 oracle against facts that do not come from the oracle itself.
 
 * the cache-statistics example the pages print (golden fixture);
+* the visible page order (scale -> window -> specials, the window oldest first, the
+  specials in the order they were opened, streams in index order) of two small
+  streams worked by hand, frame by frame (golden fixture);
 * closed forms of the visible set (patch pages, special tokens, last page length);
 * bookkeeping invariants (page conservation, no duplicate ids, specials never leave);
 * brute force: dense attention over the whole frame history, sliced by the window
@@ -76,6 +79,28 @@ def pin_golden_stats():
         st.append()
         st.evict()
     assert st.stats() == g["expected"], st.stats()
+
+
+def pin_page_order():
+    """Visible page tables of the hand-worked streams in tests/golden/visible_page_order.json."""
+    with open(os.path.join(GOLDEN, "visible_page_order.json")) as fh:
+        g = json.load(fh)
+    for case in ("single_stream", "two_streams"):
+        s = g[case]["setup"]
+        B, mpp, msp = s["num_streams"], s["max_patch_pages"], s["max_special_pages"]
+        streams = []
+        for b in range(B):
+            pids, sids = oracle.default_page_ids(B, mpp, msp, b)
+            streams.append(oracle.StreamPages(patches_per_frame=s["patches_per_frame"],
+                                              specials_per_frame=s["specials_per_frame"], page_size=s["page_size"],
+                                              scale_frames=s["scale_frames"], sliding_window=s["sliding_window"],
+                                              patch_ids=pids, special_ids=sids))
+        T = s["patches_per_frame"] + s["specials_per_frame"]
+        for want in g[case]["after_frame"]:
+            step(streams)
+            p = oracle.plan(streams, T)
+            for key in ("indices", "kv_indptr", "last_page_len", "num_patch_pages", "qo_indptr"):
+                assert p[key] == want[key], f"{case} frame {want['frame']}: {key} {p[key]} != {want[key]}"
 
 
 def closed_form(cfg, f):
@@ -313,6 +338,7 @@ def pin_rope_properties(seed=5):
 
 PINS = {
     "golden_stats": pin_golden_stats,
+    "page_order": pin_page_order,
     "closed_forms": lambda: [pin_closed_forms(c) for c in SMALL_VARIANTS],
     "brute_force": lambda: [pin_brute_force(c, i) for i, c in enumerate(SMALL_VARIANTS)],
     "permutation": pin_permutation,
@@ -328,6 +354,10 @@ PINS = {
 
 def test_golden_stats_example():
     pin_golden_stats()
+
+
+def test_visible_page_order_worked_by_hand():
+    pin_page_order()
 
 
 @pytest.mark.parametrize("idx", range(len(SMALL_VARIANTS)))
@@ -498,6 +528,34 @@ def _rollback_keeps_special_pages(self):
     self.undo = None
 
 
+def _pages_specials_first(self):
+    return list(self.special_pages) + list(self.scale) + list(self.live)
+
+
+def _pages_window_reversed(self):
+    return list(self.scale) + list(reversed(self.live)) + list(self.special_pages)
+
+
+def _pages_scale_after_window(self):
+    return list(self.live) + list(self.scale) + list(self.special_pages)
+
+
+def _pages_specials_reversed(self):
+    return list(self.scale) + list(self.live) + list(reversed(self.special_pages))
+
+
+def _pages_window_by_id(self):
+    return list(self.scale) + sorted(self.live) + list(self.special_pages)
+
+
+def _plan_streams_reversed(streams, tokens_per_frame):
+    p = _ORIG_PLAN(list(reversed(streams)), tokens_per_frame)
+    return p
+
+
+_ORIG_PLAN = opc.plan
+
+
 _ORIG_PAIR_ANGLES = orope.pair_angles
 
 
@@ -530,6 +588,12 @@ _ORIG_ROTATE = orope.rotate
 
 
 MUTATIONS = {
+    "specials_listed_first": (opc.StreamPages, "visible_pages", _pages_specials_first),
+    "window_listed_newest_first": (opc.StreamPages, "visible_pages", _pages_window_reversed),
+    "scale_listed_after_window": (opc.StreamPages, "visible_pages", _pages_scale_after_window),
+    "special_pages_reversed": (opc.StreamPages, "visible_pages", _pages_specials_reversed),
+    "window_sorted_by_page_id": (opc.StreamPages, "visible_pages", _pages_window_by_id),
+    "streams_planned_in_reverse": (opc, "plan", _plan_streams_reversed),
     "rope_turns_backwards": (orope, "rotate", _rotate_backwards),
     "rope_half_split_pairs": (orope, "rotate", _rotate_half_split),
     "rope_frequency_exponent_doubled": (orope, "pair_angles", _angles_full_dim_exponent),
@@ -552,8 +616,8 @@ MUTATIONS = {
 def test_planted_mistake_is_caught(name, monkeypatch):
     obj, attr, fn = MUTATIONS[name]
     monkeypatch.setattr(obj, attr, fn)
-    # the package re-exports attend/merge: patch those too
-    if obj is oatt:
+    # the package re-exports attend/merge/plan: patch those too
+    if obj is oatt or obj is opc:
         monkeypatch.setattr(oracle, attr, fn)
     caught = []
     for pin_name, pin in PINS.items():
