@@ -272,7 +272,8 @@ def run_reference(args, w: wl.Workload):
     sample = (f"per step: one frame of bookkeeping + gather + fp64 attention of block 0 over {heads} of "
               f"{w.num_heads} heads at frame {frame} ({visible_tokens(w, frame)} visible keys); "
               f"frame-steps/s extrapolated x{w.num_heads // heads} heads x{w.num_blocks} blocks; "
-              f"{len(times)} steps timed")
+              f"{len(times)} steps timed; ms_per_step is 1000/value, i.e. extrapolated the same way, "
+              f"not a timed full step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
         "steps": len(times), "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -303,7 +304,7 @@ def run_gpu(args, w: wl.Workload):
     if world > 1:
         dist_init("nccl")
     import streaming_paged_kv_two_gb300 as spk
-    from gpu_harness import spk_config_for, to_device
+    from workload_device import spk_config_for, to_device
 
     K, W = args.steps, args.warmup
     total_frames = w.frames
@@ -593,7 +594,7 @@ def run_prefill(args, w: wl.Workload):
     if world > 1:
         dist_init("nccl")
     import streaming_paged_kv_two_gb300 as spk
-    from gpu_harness import spk_config_for, to_device
+    from workload_device import spk_config_for, to_device
 
     F, K, W = args.query_frames, args.steps, args.warmup
     wk = w.replace(frames=F)

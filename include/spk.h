@@ -104,6 +104,9 @@ typedef struct {
   int32_t num_ctas;        /* CTAs of one attention launch */
   int32_t merge_needed;    /* 1 when some stream has more than one split (merge kernel runs) */
   int64_t visible_tokens;  /* sum over streams of visible keys */
+  int64_t split_scratch_bytes;     /* bytes of split-KV partials this plan writes (0 when no merge
+                                      runs); spk_run_attention_static_scratch needs them to fit */
+  int64_t static_scratch_capacity; /* bytes of the library's static split-KV array */
 } spk_plan_info;
 
 typedef struct spk_cache spk_cache;
@@ -116,7 +119,10 @@ const char* spk_last_error(void);
  * Either output pointer may be NULL.  No CUDA call. */
 int spk_required_bytes(const spk_config* cfg, size_t* pool_bytes_per_block, size_t* workspace_bytes);
 
-/* Create a cache.  pools: host array of num_blocks device pointers, or NULL for a
+/* Create a cache ("How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D
+ * Reconstruction", "Initializing the Cache Manager" and "Physical Memory Layout": one
+ * pool [max_num_pages, 2, page_size, H, D] per block, page ids shared by every block).
+ * pools: host array of num_blocks device pointers, or NULL for a
  * bookkeeping-only cache.  The library keeps the pointers (the caller keeps
  * ownership) and zeroes every pool once, on the legacy default stream, before
  * returning, so slots that are never written read as 0.  Builds one TMA
@@ -127,10 +133,16 @@ int spk_create_cache(const spk_config* cfg, void* const* pools, spk_cache** out)
 int spk_destroy_cache(spk_cache* cache);
 
 /* Clear the bookkeeping (free lists back to their initial order, counters to zero);
- * the pools are kept as they are ("Resetting for New Sequences"). */
+ * the pools are kept as they are ("How Paged KV Cache Attention Achieves Stable
+ * Inference in Ling-Bot-Map", "Resetting for New Sequences"). */
 int spk_reset(spk_cache* cache);
 
-/* Append one frame's K/V for one block.  k, v: device [T, H, D] contiguous NHD in
+/* Append one frame's K/V for one block ("How Paged KV Cache Attention Achieves Stable
+ * Inference in Ling-Bot-Map", "Frame Appending Without Dispatch Overhead": direct
+ * writes into the frame's slots; "How FlashInfer's Paged KV Cache Attention
+ * Outperforms SDPA Fallback in Streaming Inference", "Two-Stream Design": one patch
+ * page per frame, special tokens packed over append-only pages).
+ * k, v: device [T, H, D] contiguous NHD in
  * the cache dtype, rows 0..P-1 patch tokens, rows P..T-1 special tokens.
  * block 0 starts a new frame: it takes a free patch page (a scale page while
  * fewer than scale_frames exist, else a live-window page) and reserves S special
@@ -180,7 +192,9 @@ int spk_append_frame_rope(spk_cache* cache, int stream, int block, const void* k
                           void* cuda_stream);
 
 /* Evict: move the oldest live-window pages to the free list until at most
- * sliding_window remain.  Host only, no data moves.  Marks the plan stale. */
+ * sliding_window remain ("How Paged KV Cache Attention Achieves Stable Inference in
+ * Ling-Bot-Map", "Sliding-Window Eviction Strategy": page ids move, no data is
+ * copied).  Host only.  Marks the plan stale. */
 int spk_evict_frames(spk_cache* cache, int stream);
 
 /* Deferred eviction ("How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D
@@ -203,7 +217,11 @@ int spk_set_defer_eviction(spk_cache* cache, int stream, int on);
  * evicted (defer eviction to keep it).  Marks the plan stale.  Host only. */
 int spk_rollback_frame(spk_cache* cache, int stream);
 
-/* Plan the current frame for every stream: visible page table, indptr,
+/* Plan the current frame for every stream ("How LingBot-Map Uses FlashInfer KV Cache
+ * for Streaming 3D Reconstruction", "Page Table Planning and Reuse": one plan per
+ * frame, ordered scale -> window -> specials, reused by every block; "How Paged KV
+ * Cache Attention Achieves Stable Inference in Ling-Bot-Map", "Visible Page Table
+ * Construction" and "Kernel Dispatch and Sequence Lengths"): visible page table, indptr,
  * last_page_len, patch-page counts, KV chunks and the split-KV work list.  Built on
  * the host and uploaded with one async copy into `workspace` on cuda_stream; the
  * same plan serves every block until the next append(block 0) or evict.  Every
@@ -225,7 +243,11 @@ int spk_plan(spk_cache* cache, void* workspace, void* cuda_stream);
  * else SPK_ERR_INVALID_ARG / SPK_ERR_BAD_STATE. */
 int spk_plan_queries(spk_cache* cache, int query_frames, void* workspace, void* cuda_stream);
 
-/* Attention of the current frame for one block, all streams in one launch.
+/* Attention of the current frame for one block, all streams in one launch ("How
+ * LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "Attention
+ * Kernel Execution": exact softmax(Q K^T / sqrt(D)) V over the visible keys, non-causal;
+ * "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback in Streaming
+ * Inference", "Memory Bandwidth Efficiency": only the visible pages are read).
  * q: device [B*T, H, D] (stream s owns rows s*T..s*T+T-1), out: device [B*T, H, D],
  * both in the cache dtype; with spk_plan_queries, T stands for query_frames * T.
  * workspace must be the one given to the plan.  Launches the attention kernel and,
@@ -245,10 +267,15 @@ int spk_run_attention(spk_cache* cache, int block, const void* q, void* out, voi
  * allocator.  The plan tables are still read from `workspace`, the buffer given to
  * spk_plan.  The pages describe no counterpart: this is a property of this
  * library's interface only.
- *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *   - spk_create_cache looks up the array's device address, with the cache's device
+ *     current; that is when the array's module is loaded and its 32 MiB reserved.
+ *     A call made while another device is current returns SPK_ERR_INVALID_ARG.
  *   - A plan whose partials exceed the array (splits * H * T * (D + 1) * 4 bytes,
- *     rounded up) returns SPK_ERR_INVALID_ARG; lower spk_config.splits_per_stream.
+ *     rounded up; spk_plan_info.split_scratch_bytes after spk_plan, against
+ *     spk_plan_info.static_scratch_capacity) returns SPK_ERR_INVALID_ARG and launches
+ *     nothing.  With splits_per_stream = 0 the planner's split count grows with the
+ *     visible keys, so a stream with many query rows (large T) can outgrow the array
+ *     part way through; force splits_per_stream to keep it within bounds.
  *   - Every call on a device shares the array and leaves its contents behind.
  *     Nothing in it needs to start at zero: each partial is written before it is
  *     read.  Calls whose GPU work overlaps (other streams, other caches) race on
@@ -257,10 +284,14 @@ int spk_run_attention_static_scratch(spk_cache* cache, int block, const void* q,
                                      void* cuda_stream);
 
 /* Copy one raw page [2, page_size, H, D] of block's pool to dst (host or device
- * memory, page_bytes = 2*ps*H*D*elem).  Synchronizes cuda_stream before returning. */
+ * memory, page_bytes = 2*ps*H*D*elem), for tests ("How FlashInfer's Paged KV Cache
+ * Attention Outperforms SDPA Fallback in Streaming Inference", "Physical Memory
+ * Layout").  Synchronizes cuda_stream before returning. */
 int spk_read_kv(spk_cache* cache, int block, int page_id, void* dst, void* cuda_stream);
 
-/* Host copy of the last plan.  indices has room for `capacity` entries; kv_indptr
+/* Host copy of the last plan: the tables the pages' planner hands its kernel
+ * ("How LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "Page
+ * Table Planning and Reuse").  indices has room for `capacity` entries; kv_indptr
  * and qo_indptr [B+1]; last_page_len and num_patch_pages [B].  *nnz receives the
  * number of indices even when capacity is too small (then SPK_ERR_INVALID_ARG).
  * Array pointers other than nnz may be NULL to skip them. */
@@ -276,7 +307,8 @@ int spk_get_plan_info(const spk_cache* cache, spk_plan_info* info);
 int spk_get_frame_targets(const spk_cache* cache, int stream, int32_t* patch_page,
                           int32_t* special_pages, int32_t* special_slots);
 
-/* get_cache_stats() of one stream. */
+/* get_cache_stats() of one stream ("How FlashInfer's Paged KV Cache Attention
+ * Outperforms SDPA Fallback in Streaming Inference", "Inspecting Cache Statistics"). */
 int spk_get_stats(const spk_cache* cache, int stream, spk_stats* stats);
 
 /* Synchronize cuda_stream, read and clear the device status word at the start of
@@ -288,31 +320,6 @@ int spk_read_device_status(void* workspace, void* cuda_stream, int32_t* code);
  * signals, gives up after limit_ns nanoseconds, records the timeout in the status
  * word of `workspace` and returns normally.  Read it with spk_read_device_status. */
 int spk_selftest_wait_timeout(void* workspace, int64_t limit_ns, void* cuda_stream);
-
-/* Diagnostics for the bf16 tensor-core kernel: run block's attention launch in
- * score-dump mode.  Every CTA stops after the first chunk of its KV split and writes
- * the raw Q K^T tiles of that chunk (fp32, before scaling and masking) for its up to
- * two 128-row main query tiles to dst[cta][tile][row][key] (rows and keys 0..127;
- * rows past T come from zero queries; a tile slot the CTA does not own is left as
- * is).  cta = (split * H + head) * groups + group, where a group covers query rows
- * [256*group, 256*group + 256).  dst: device memory of num_ctas * 2 * 128 * 128 * 4
- * bytes (num_ctas from spk_get_plan_info).  out is not written; same preconditions
- * as spk_run_attention. */
-int spk_debug_dump_scores(spk_cache* cache, int block, const void* q, float* dst, void* workspace,
-                          void* cuda_stream);
-
-/* Diagnostics for the bf16 tensor-core kernel: run block's attention exactly as
- * spk_run_attention does (same outputs) while the first CTA records the SM clock
- * (clock64) of its pipeline events for each of its first `capacity` chunks into
- * trace[event][chunk] (device memory, 20 * capacity uint64).  Events, in order:
- * TMA issue, MMA (tile 0) sees K/V landed, S0 keys 0..63 issued, its P seen, S1 keys
- * 0..63 issued, its P seen, tail S^T issued, tail P seen, S0 keys 64..127 issued, its
- * P seen, K/V stage released by tile 0, softmax 0 sees S (keys 0..63), softmax 0
- * signals P, softmax 1 sees S (keys 0..63), softmax 1 signals P, tail sees S^T, tail
- * signals P, softmax 0 sees S (keys 64..127), softmax 0 signals P, K/V landed in
- * shared memory.  Entries of events that do not happen are left as they were. */
-int spk_debug_trace_attention(spk_cache* cache, int block, const void* q, void* out, void* workspace,
-                              uint64_t* trace, int32_t capacity, void* cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -59,7 +59,8 @@ class spk_rope(ctypes.Structure):
 
 class spk_plan_info(ctypes.Structure):
     _fields_ = [("num_chunks", ctypes.c_int32), ("num_splits", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
-                ("merge_needed", ctypes.c_int32), ("visible_tokens", ctypes.c_int64)]
+                ("merge_needed", ctypes.c_int32), ("visible_tokens", ctypes.c_int64),
+                ("split_scratch_bytes", ctypes.c_int64), ("static_scratch_capacity", ctypes.c_int64)]
 
 
 def _load():

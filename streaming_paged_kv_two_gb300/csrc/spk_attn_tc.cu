@@ -835,17 +835,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
+cudaError_t configure_tc() {
+  return cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kLaunch);
+}
+
+template <int D>
 cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t s) {
   constexpr int smem = Cfg<D>::kLaunch;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   const int64_t grid = int64_t(p.num_splits) * p.H * p.ngroups;
   if (grid <= 0 || grid > 0x7fffffff) return cudaErrorInvalidValue;
   attention_tc_kernel<D><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
@@ -853,6 +849,11 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t 
 }
 
 }  // namespace
+
+cudaError_t configure_attention_bf16() {
+  cudaError_t e = configure_tc<64>();
+  return e != cudaSuccess ? e : configure_tc<128>();
+}
 
 cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s) {
   return p.D == 64 ? launch_tc<64>(p, kv_map, s) : launch_tc<128>(p, kv_map, s);

@@ -17,6 +17,7 @@
 // so that one attention launch fills the GPU; the split results are combined by
 // a log-sum-exp merge.
 #include "spk.h"
+#include "spk_debug.h"
 #include "spk_internal.h"
 
 #include <cudaTypedefs.h>
@@ -182,6 +183,9 @@ struct spk_cache {
   bool staged_used[2] = {false, false};
   int stage_idx = 0;
   long long wait_limit_ns = kDefaultWaitLimitNs;
+  // device address of the library's static split-KV array on this cache's device,
+  // looked up when the cache is created (spk_run_attention_static_scratch)
+  void* static_scratch = nullptr;
 };
 
 namespace {
@@ -297,6 +301,15 @@ int choose_splits(const spk_cache* c, const std::vector<int32_t>& nchunks, std::
   return SPK_OK;
 }
 
+// Bytes of split-KV partials of the current plan's launch shape: fp32 O [splits][H][Tq][D]
+// (256-byte aligned), then fp32 lse [splits][H][Tq].
+size_t split_scratch_o_bytes(const spk_cache* c) {
+  return align256(size_t(c->info.num_splits) * c->cfg.num_heads * c->Tq * c->cfg.head_dim * sizeof(float));
+}
+size_t split_scratch_bytes(const spk_cache* c) {
+  return split_scratch_o_bytes(c) + size_t(c->info.num_splits) * c->cfg.num_heads * c->Tq * sizeof(float);
+}
+
 int build_plan(spk_cache* c) {
   const spk_config& g = c->cfg;
   const int B = g.num_streams;
@@ -353,6 +366,8 @@ int build_plan(spk_cache* c) {
                      (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->Tq, g.head_dim).ngroups : (c->Tq + 7) / 8);
   c->info.merge_needed = merge ? 1 : 0;
   c->info.visible_tokens = visible;
+  c->info.split_scratch_bytes = merge ? int64_t(split_scratch_bytes(c)) : 0;
+  c->info.static_scratch_capacity = int64_t(static_scratch_bytes());
   return SPK_OK;
 }
 
@@ -444,7 +459,13 @@ int spk_create_cache(const spk_config* cfg, void* const* pools, spk_cache** out)
       e = cudaEventCreateWithFlags(&c->staged[i], cudaEventDisableTiming);
       if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
     }
+    // The static split-KV array's module is loaded here, at set-up, with the cache's device
+    // current: spk_run_attention_static_scratch then reserves nothing when it runs.
+    e = static_scratch_address(&c->static_scratch);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "static scratch address"));
     if (cfg->dtype == SPK_BF16) {
+      e = configure_attention_bf16();
+      if (e != cudaSuccess) return bail(cuda_fail(e, "attention kernel configuration"));
       auto encode = get_encode_fn();
       if (!encode) return bail(fail(SPK_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable"));
       c->maps.resize(cfg->num_blocks);
@@ -813,18 +834,20 @@ int spk_run_attention_static_scratch(spk_cache* c, int block, const void* q, voi
   for (int s = 0; s < g.num_streams; ++s)
     if (!c->st[s].appended[block])
       return fail(SPK_ERR_BAD_STATE, "block %d of stream %d not appended in the current frame", block, s);
-  // partials of every split: fp32 O [splits][H][T][D], then fp32 lse [splits][H][T] (256-byte aligned)
-  const size_t rows = size_t(c->info.num_splits) * g.num_heads * c->Tq;
-  const size_t o_bytes = align256(rows * g.head_dim * sizeof(float));
-  const size_t need = o_bytes + rows * sizeof(float);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != c->device)
+    return fail(SPK_ERR_INVALID_ARG, "device %d is current but the cache lives on device %d", dev, c->device);
+  // partials of every split: fp32 O, then fp32 lse (split_scratch_bytes)
+  const size_t o_bytes = split_scratch_o_bytes(c);
+  const size_t need = split_scratch_bytes(c);
   if (need > static_scratch_bytes())
     return fail(SPK_ERR_INVALID_ARG,
                 "this plan needs %zu bytes of split scratch but the static array holds %zu; "
                 "use fewer KV splits (spk_config.splits_per_stream)",
                 need, static_scratch_bytes());
-  void* scratch = nullptr;
-  cudaError_t e = static_scratch_address(&scratch);
-  if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+  void* scratch = c->static_scratch;
   char* ws = static_cast<char*>(workspace);
   const AttnParams p = attention_params(c, block, q, out, ws, static_cast<float*>(scratch),
                                         reinterpret_cast<float*>(static_cast<char*>(scratch) + o_bytes));

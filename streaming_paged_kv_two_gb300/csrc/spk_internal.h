@@ -141,6 +141,9 @@ struct MergeParams {
 cudaError_t launch_append(const AppendParams& p, int elem_bytes, cudaStream_t s);
 cudaError_t launch_append_rope(const AppendRopeParams& p, int elem_bytes, cudaStream_t s);
 cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s);
+// Once per cache, with its device current: kernel attributes (dynamic shared memory) of the
+// bf16 attention kernels.
+cudaError_t configure_attention_bf16();
 cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s);

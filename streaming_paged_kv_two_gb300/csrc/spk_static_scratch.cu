@@ -27,7 +27,9 @@ std::mutex g_scratch_mu;
 size_t static_scratch_bytes() { return kScratchBytes; }
 
 // Device address of the array on the current device.  The first call on a device
-// resolves it with cudaGetSymbolAddress (with that device current) and keeps it.
+// resolves it with cudaGetSymbolAddress (with that device current) and keeps it; the
+// library makes that call when a cache is created, so the module holding the array is
+// loaded (and its memory reserved) at set-up rather than by the first attention call.
 cudaError_t static_scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -7,28 +7,11 @@ import torch
 
 import workloads as wl
 import streaming_paged_kv_two_gb300 as spk
+from workload_device import spk_config_for, to_device  # noqa: F401  (re-exported for the tests)
 
 BF16_MAX_ABS = 2e-2
 BF16_MEAN_ABS = 2e-3
 F32_MAX_ABS = 1e-4
-
-
-def spk_config_for(w: wl.Workload, splits: int = 0, max_query_frames: int = 0):
-    po, so = wl.page_orders(w)
-    return spk.make_config(
-        num_blocks=w.num_blocks, num_streams=w.num_streams, num_heads=w.num_heads, head_dim=w.head_dim,
-        page_size=w.page_size, patches_per_frame=w.patches_per_frame, specials_per_frame=w.specials_per_frame,
-        scale_frames=w.scale_frames, sliding_window=w.sliding_window, max_patch_pages=w.max_patch_pages,
-        max_special_pages=w.max_special_pages, dtype=spk.SPK_BF16 if w.dtype == "bf16" else spk.SPK_F32,
-        splits_per_stream=splits, max_query_frames=max_query_frames,
-        patch_page_order=None if po is None else po.tolist(),
-        special_page_order=None if so is None else so.tolist())
-
-
-def to_device(x: np.ndarray, dtype: str) -> torch.Tensor:
-    if dtype == "bf16":
-        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.bfloat16)
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
