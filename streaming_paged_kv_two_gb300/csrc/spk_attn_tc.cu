@@ -19,19 +19,17 @@
 //               buffers in TMEM, so Q K^T of the next half chunk runs on the tensor
 //               core while the softmax works on the current one.  fp32 online
 //               softmax in log2 units: a half's scores are exponentiated against the
-//               running max while their own max is taken, and only when that max
-//               exceeds the running one by more than a threshold (2 for D = 64, whose
-//               exponentials are taken on bf16-rounded argument pairs, 2^8 for
-//               D = 128) is O rescaled in TMEM and the half recomputed; masking of
-//               the chunk's ragged tail; P written back as bf16 over S; row sums
-//               taken from the rounded P that the MMA consumes.
+//               running max m and the packed bf16 P words are OR-ed together; only
+//               when one of them reaches 2.0 (a score more than 1 above m) does the
+//               warp move m, rescale O in TMEM and recompute the half.  Masking of
+//               the chunk's ragged tail; P written back as bf16 over S.
 //   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
 //               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
-//               every tail row; warp q owns keys [32q, 32q+32) of each chunk and keeps
-//               its own (max, sum, O) per row.  Its P goes to rows 16q.. of a 64-row
-//               shared-memory tile; one O2 += P2 V MMA with M = 64 (whose rows
-//               16q..16q+15 live in TMEM lane quarter q) accumulates the four partial
-//               states side by side; they are merged at the end.
+//               every tail row; warp q owns keys [32q, 32q+32) of each chunk.  The four
+//               warps share one running max per row (moved, rarely, after a barrier
+//               that ORs their "score above the max" flags), so one
+//               O2^T += V^T P2^T (M = 64 columns of V, N = 8 rows, K = 128 keys, P2
+//               from shared memory) accumulates a whole chunk.
 //   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
 //               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
 //               swizzle, into a ring of shared-memory stages.
@@ -41,35 +39,45 @@
 //               N=D, K=64) followed by Q K^T of half g+2 into the buffer just read.
 //               The consumers advance independently; a K/V stage is released once
 //               every consumer is done with it.
-// TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) | O0 | O1, then for D = 64
-// O2 (64) | S2^T[0] | S2^T[1] (16 each).  With D = 64 the PV MMA's B operand is V
-// extended by a 16-column block of ones in shared memory, so O0/O1 are 80 columns wide
-// and column 64 accumulates the row sum of the bf16 P that the MMA consumed.
+// head_dim 64: Q_t is the TMEM A operand of Q K^T (only K is read from shared memory),
+// and the PV MMA's B operand is V extended by a 16-column block of ones in shared
+// memory, so O0/O1 are 80 columns wide and column 64 accumulates the row sum of the bf16
+// P that the MMA consumed.  TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each)
+// | O0 | O1 (80 each) | Q0 | Q1 (32 each) | S2^T (16) | O2^T (8).
+// head_dim 128: Q in shared memory; S (4 x 64) | O0 | O1 (128 each); fp32 row sums.
+// Key rows past a ragged chunk's length are zeroed in the V tile before a PV MMA reads
+// them, so whatever a slot past the valid tokens holds (a rolled-back frame, an earlier
+// stream) cannot reach the output, not even as 0 * Inf.
 // The epilogue writes bf16 output (one split) or an fp32 partial with its log2
 // log-sum-exp (several splits, combined by the merge kernel).
-// Every wait is bounded: on timeout the kernel records a status word, drains its
-// own copies and MMAs, frees TMEM and returns.
+// Every mbarrier wait is bounded: on timeout the kernel records a status word, drains
+// its own copies and MMAs, frees TMEM and returns.
+// kDiag instantiations carry the diagnostics (score dump, event trace); the kernel that
+// spk_run_attention launches is compiled without them.
 #include "ptx_sm100.cuh"
 #include "spk_internal.h"
 
 #include <cuda_bf16.h>
 
-#include <type_traits>
-
 namespace spk {
 namespace {
 
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
-constexpr int kP2ColBlockBytes = 64 * 128;  // the tail's 64-row P tile: one column block
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kTailMaxRows = 8;            // rows of the tail (the transposed tail MMA has N = 16)
-constexpr int kTailN = 16;
+constexpr int kTailMaxRows = 8;            // rows of the tail (N of O2^T)
+constexpr int kTailN = 16;                 // N of S2^T (M = 128 needs N >= 16)
+constexpr int kP2Bytes = kTailMaxRows * 256;  // one tail P tile: 8 rows x 128 keys bf16 (two 1 KB column blocks)
 constexpr int kHalfKeys = 64;              // keys per main-tile score buffer
 constexpr int kThreads = 512;
 constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;   // warps 13, 14, 15 issue the MMAs of main tile 0, main tile 1 and the tail
 constexpr int kSoftmaxThreads = 384;  // warps 0-11 (all arrive on q_full)
+// A packed bf16 P word has bit 14 or bit 30 set when one of its two values is >= 2.0
+// (or not finite): the score lies more than 1 (log2 units) above the running max.
+constexpr uint32_t kPHighBits = 0x40004000u;
+constexpr float kThreshold = 1.0f;  // the same bound for the tail's fp32 check
+
+constexpr int align1024(int x) { return (x + 1023) & ~1023; }
 
 template <int D>
 struct Cfg {
@@ -78,35 +86,33 @@ struct Cfg {
   // D == 64: the row sums come out of the PV MMA, whose B operand is V extended by a
   // 16-column block of ones (O gets 16 more columns, each holding the row sum)
   static constexpr bool kOnes = (D == 64);
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kQ0 = 0;
+  // D == 64: Q lives in TMEM as the A operand of Q K^T
+  static constexpr bool kQTmem = (D == 64);
+  static constexpr int kStages = (D == 64) ? 6 : 2;
+  // shared memory
+  static constexpr int kQ0 = 0;          // D == 128: the two Q tiles
   static constexpr int kQ1 = kTile;
-  static constexpr int kQ2 = 2 * kTile;                 // tail Q: kTailN rows x 128 bytes (D == 64)
-  static constexpr int kP2 = kQ2 + 2048;                // two tail P tiles: 64 rows x 128 keys bf16 each
-  static constexpr int kP2Bytes = 2 * kP2ColBlockBytes;
-  static constexpr int kKV = kTail ? kP2 + 2 * kP2Bytes : 2 * kTile;
+  static constexpr int kQ2 = 0;          // D == 64: tail Q, 16 rows x 128 bytes
+  static constexpr int kP2 = 2048;       // D == 64: two tail P tiles
+  static constexpr int kKV = kTail ? align1024(kP2 + 2 * kP2Bytes) : 2 * kTile;
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kOnesBlk = kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones (kOnes)
-  static constexpr int kBars = kOnesBlk + (kOnes ? kColBlockBytes : 0);
-  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full[2],
-  // p2_ready[2], pv2_done
+  static constexpr int kTailX = kOnesBlk + (kOnes ? kColBlockBytes : 0);  // tail exchange: [2][4][8] maxima, [2][4] flags
+  static constexpr int kBars = kTailX + (kTail ? 2 * 4 * (kTailMaxRows + 1) * 4 + 32 : 0);
+  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full,
+  // s2_free, p2_ready[2], pv2_done
   static constexpr int kNumBars = 2 * kStages + 19;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kOW = D + (kOnes ? 16 : 0);  // TMEM columns of a main tile's O
-  // The main softmax moves its running max when a score exceeds it by more than this
-  // (log2 units): 2^8 with fp32 exponentials; 2^2 with paired bf16 ones (D = 64), which
-  // bounds the argument's bf16 rounding.
-  static constexpr float kThreshold = kOnes ? 2.0f : kRescaleThreshold;
   static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + kOW;
-  static constexpr uint32_t kO2 = 4 * kHalfKeys + 2 * kOW, kS2 = kO2 + 64;  // D == 64 only: O2, S2^T[2]
-  static_assert(kTail ? kS2 + 2 * kTailN <= 512 : kO1 + kOW <= 512, "TMEM budget");
-  static_assert(kTailN * 128 <= kP2 - kQ2, "tail Q tile");
+  static constexpr uint32_t kTQ0 = kO1 + kOW, kTQ1 = kTQ0 + D / 2;   // D == 64: Q0, Q1 as bf16 pairs
+  static constexpr uint32_t kS2 = kTQ1 + D / 2, kO2 = kS2 + kTailN;  // D == 64: S2^T, O2^T
+  static_assert(kTail ? kO2 + kTailMaxRows <= 512 : kO1 + kOW <= 512, "TMEM budget");
   static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kOnesBlk % 1024 == 0,
                 "128-byte-swizzled tiles start on 1024-byte boundaries");
-  static_assert(kStages * kStageBytes >= 4 * kTailMaxRows * (64 + 2) * 4, "tail merge scratch");
-  static_assert(kTailMaxRows <= 16, "a key group's tail rows fit the 16 rows of its M = 64 quarter");
+  static_assert(!kTail || kQ2 + 2048 <= kP2, "tail Q tile");
   static_assert(kLaunch <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -114,10 +120,15 @@ struct Cfg {
 __device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(kHalfKeys * (2 * t + b)); }
 
 // Trace mode (diagnostics): CTA 0 records the SM clock of an event for a chunk.
+template <bool kDiag>
 __device__ __forceinline__ void trace_at(const AttnParams& p, int ev, int chunk, long long clk) {
-  if (p.trace != nullptr && blockIdx.x == 0 && chunk < p.trace_cap) p.trace[int64_t(ev) * p.trace_cap + chunk] = clk;
+  if constexpr (kDiag)
+    if (p.trace != nullptr && blockIdx.x == 0 && chunk < p.trace_cap) p.trace[int64_t(ev) * p.trace_cap + chunk] = clk;
 }
-__device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) { trace_at(p, ev, chunk, clock64()); }
+template <bool kDiag>
+__device__ __forceinline__ void trace(const AttnParams& p, int ev, int chunk) {
+  if constexpr (kDiag) trace_at<kDiag>(p, ev, chunk, clock64());
+}
 
 __device__ __forceinline__ void signal_abort(int32_t* status, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -142,11 +153,10 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Byte address of element (row, key) of the tail's P tile: 64 rows x 128 keys bf16,
-// K-major, 128-byte swizzle, keys 0-63 and 64-127 in two 8 KB column blocks.
+// Byte address of element (row, key) of a tail P tile: 8 rows x 128 keys bf16, K-major,
+// 128-byte swizzle, keys 0-63 and 64-127 in two 1 KB column blocks.
 __device__ __forceinline__ uint32_t p2_addr(uint32_t base, int row, int key) {
-  return base + uint32_t((key >> 6) * kP2ColBlockBytes + (row >> 3) * 1024 + (row & 7) * 128 +
-                         ((((key & 63) >> 3) ^ (row & 7)) << 4) + (key & 7) * 2);
+  return base + uint32_t((key >> 6) * 1024 + row * 128 + ((((key & 63) >> 3) ^ row) << 4) + (key & 7) * 2);
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
@@ -155,6 +165,25 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
 
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Zero key rows [r0, r1) of a 128-key V tile (D/64 column blocks of 128-byte rows; the
+// swizzle only permutes 16-byte pieces inside a row, so a whole row is zeroed as it
+// lies) with `nthreads` threads, this one being `tid`.
+template <int D>
+__device__ __forceinline__ void zero_v_rows(uint32_t sv, int r0, int r1, int tid, int nthreads) {
+  const int units = (r1 - r0) * 8;  // 16-byte pieces per column block
+  for (int i = tid; i < units * (D / 64); i += nthreads) {
+    const int cb = i / units, u = i - cb * units;
+    st_shared_zero16(sv + uint32_t(cb * kColBlockBytes + (r0 + (u >> 3)) * 128 + (u & 7) * 16));
+  }
+}
+
+// a | b | c in one instruction
+__device__ __forceinline__ uint32_t or3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 // Store one row of a 128-row Q tile in K-major 128-byte-swizzled layout: 16-byte
@@ -173,11 +202,13 @@ __device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src
 }
 
 // p = 2^(s*sl2 - m) for the 64 fp32 scores of a half chunk (two 32-column quarters),
-// packed to bf16 pairs in pk; returns the fp32 sum of the rounded values when kSum.  The
-// argument is one packed fp32x2 FMA per pair and the sum adds the two bf16 halves directly.
+// packed to bf16 pairs in pk.  kSum: fp32 exponentials, one rounding, and the fp32 sum
+// of the rounded values is returned; otherwise exponentials of the bf16-rounded
+// argument pairs (the row sums come from the PV MMA) and 0 is returned.  *orr receives
+// the OR of the packed words (their high exponent bits flag a value >= 2).
 template <bool kSum>
 __device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* sb, float sl2, float neg_m,
-                                            uint32_t (&pk)[32]) {
+                                            uint32_t (&pk)[32], uint32_t* orr) {
   float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
@@ -189,11 +220,18 @@ __device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* 
       pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
       sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
     } else {
-      // the row sums come from the MMA: exponentiate the bf16-rounded arguments as a
-      // pair (x <= 2 here, so the argument's rounding moves p by at most 0.27 %)
+      // x < 1 unless the max moves, so the argument's bf16 rounding moves p by at most
+      // 0.14 % (at x = 1), below P's own rounding
       pk[e] = ptx::ex2_bf16x2(pack_bf16(x0, x1));
     }
   }
+  uint32_t o0 = 0, o1 = 0;
+#pragma unroll
+  for (int e = 0; e < 32; e += 4) {
+    o0 = or3(o0, pk[e], pk[e + 1]);
+    o1 = or3(o1, pk[e + 2], pk[e + 3]);
+  }
+  *orr = o0 | o1;
   return (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
 
@@ -238,32 +276,35 @@ __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float co
 }
 
 // Rare path of the online softmax (kept out of line so the hot loop's registers are
-// not spent on it), taken when some row of the warp saw a score above its running max
-// m by more than 2^8: the row moves to m_new; O (every earlier PV of this tile: when
-// o_cols > 0, wait for the previous half's PV, tracked by pv_bar) is scaled by
-// corr = 2^(m - m_new), and the half's P is recomputed from S (still in TMEM) with
-// the new offset and stored over it.  Returns the sum of the new rounded P (when
-// kSum) and whether the wait succeeded.
+// not spent on it), taken when some P value of the warp reached 2: every row that did
+// (`need`) moves its running max m to max(m, the half's max); O (every earlier PV of
+// this tile: when o_cols > 0, wait for the previous half's PV, tracked by pv_bar) is
+// scaled by corr = 2^(m - m_new), and the half's P is recomputed from S (still in TMEM)
+// with the new offset and stored over it.  Returns (m_new, sum of the new rounded P when
+// kSum, corr, 1 if the wait succeeded else 0).
 template <bool kSum>
-__device__ __noinline__ float2 move_running_max(uint32_t tO, uint32_t tS, int o_cols, float corr, float neg_m,
-                                                float sl2, int first_key, int len, uint32_t pv_bar, uint32_t parity,
+__device__ __noinline__ float4 move_running_max(uint32_t tO, uint32_t tS, int o_cols, bool need, float m, float sl2,
+                                                int first_key, int len, uint32_t pv_bar, uint32_t parity,
                                                 long long limit, const volatile int* abort_flag) {
+  uint32_t sa[32], sb[32], pk[32], orr;
+  ptx::tmem_ld32(tS, sa);
+  ptx::tmem_ld32(tS + 32, sb);
+  ptx::tmem_wait_ld();
+  mask32(sa, first_key, len);
+  mask32(sb, first_key + 32, len);
+  const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
+  const float m_new = need ? fmaxf(m, mx) : m;
+  const float corr = m_new == m ? 1.f : ptx::ex2(m - m_new);
   bool ok = true;
   if (o_cols) {
     ok = ptx::mbar_wait_warp(pv_bar, parity, limit, abort_flag);
     ptx::tc_fence_after();
     rescale_tmem(tO, o_cols, corr);
   }
-  uint32_t sa[32], sb[32], pk[32];
-  ptx::tmem_ld32(tS, sa);
-  ptx::tmem_ld32(tS + 32, sb);
-  ptx::tmem_wait_ld();
-  mask32(sa, first_key, len);
-  mask32(sb, first_key + 32, len);
-  const float sum = exp_pack64<kSum>(sa, sb, sl2, neg_m, pk);
+  const float sum = exp_pack64<kSum>(sa, sb, sl2, -m_new, pk, &orr);
   ptx::tmem_st32(tS, pk);
   ptx::tmem_wait_st();
-  return make_float2(sum, ok ? 1.f : 0.f);
+  return make_float4(m_new, sum, corr, ok ? 1.f : 0.f);
 }
 
 // Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
@@ -290,7 +331,24 @@ __device__ __forceinline__ void store_output_cols(const AttnParams& p, const Wor
   }
 }
 
-template <int D>
+// OR of a predicate over the 128 threads of the tail warps (named barrier 1): every
+// tail thread must call it the same number of times.
+__device__ __forceinline__ bool tail_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void tail_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D, bool kDiag>
 __global__ void __launch_bounds__(kThreads, 1)
     attention_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap kv_map) {
   using C = Cfg<D>;
@@ -309,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto p_ready = [&](int t, int b) { return q_full + 8 * (5 + 2 * t + b); };
   auto pv_done = [&](int t) { return q_full + 8 * (9 + t); };
   auto o_done = [&](int t) { return q_full + 8 * (11 + t); };
-  auto s2_full = [&](int b) { return q_full + 8 * (14 + b); };
+  const uint32_t s2_full = q_full + 8 * 14, s2_free = q_full + 8 * 15;
   auto p2_ready = [&](int b) { return q_full + 8 * (16 + b); };
   const uint32_t pv2_done = q_full + 8 * 18;
   const uint32_t sOnes = sbase + C::kOnesBlk;
@@ -332,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool has_tail = C::kTail && group == p.ngroups - 1 && p.tail_rows > 0;
   const int tail_row0 = p.main_tiles * kTileRows;
   const long long limit = p.wait_limit_ns;
-  const bool dump = p.dump_scores != nullptr;
+  bool dump = false;
+  if constexpr (kDiag) dump = p.dump_scores != nullptr;
   const float sl2 = p.scale_log2;
 
   if (threadIdx.x == 0) {
@@ -350,10 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(pv_done(t), 1);
     }
     for (int t = 0; t < 3; ++t) ptx::mbar_init(o_done(t), 1);
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(s2_full(b), 1);
-      ptx::mbar_init(p2_ready(b), 128);
-    }
+    ptx::mbar_init(s2_full, 1);
+    ptx::mbar_init(s2_free, 128);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(p2_ready(b), 128);
     ptx::mbar_init(pv2_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -385,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ChunkDesc cd = p.chunks[c0 + i];
         const int start = cd.start_len & 0xFFFF;
         ptx::mbar_arrive_expect_tx(full_bar(st), 2 * C::kTile);
-        trace(p, kTrTmaIssue, i);
+        trace<kDiag>(p, kTrTmaIssue, i);
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
           ptx::tma_load_4d(sK(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page, full_bar(st));
@@ -396,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = issued > S ? issued - S : 0; i < issued; ++i)  // drain: copies must land before exit
         ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, nullptr);
-    } else if (lane == 1 && p.trace != nullptr && blockIdx.x == 0) {
+    } else if (kDiag && lane == 1 && p.trace != nullptr && blockIdx.x == 0) {
       // trace mode: watch the full barriers and record when each chunk's K/V lands
       for (int i = 0; i < n; ++i)
-        if (ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, abort_flag)) trace(p, kTrLanded, i);
+        if (ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, abort_flag)) trace<kDiag>(p, kTrLanded, i);
     }
     __syncwarp();
   } else if (warp >= kWarpMma) {
@@ -411,9 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp - kWarpMma;
     const bool mine = (t < 2) ? (t < n_main) : has_tail;
     if (lane == 0 && mine) {
-      const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sQ0, 16, 1024) >> 32);
+      const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sbase, 16, 1024) >> 32);
       const uint32_t k0_lo = uint32_t(ptx::smem_desc_sw128(sK(0), 16, 1024));
-      // V as an MN-major B operand: the leading offset is the distance to the next 64-column
+      // V as an MN-major operand: the leading offset is the distance to the next 64-column
       // block (V's second half when D = 128, the ones block when the row sums ride along)
       auto v_lo_of = [&](int st) {
         return uint32_t(ptx::smem_desc_sw128(sV(st), C::kOnes ? sOnes - sV(st) : kColBlockBytes, 1024));
@@ -426,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, kHalfKeys, 0, 0);
         constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, C::kOW, 0, 1);
         const uint32_t q_lo = uint32_t(ptx::smem_desc_sw128(t ? sQ1 : sQ0, 16, 1024));
+        const uint32_t tQ = tmem + (t ? C::kTQ1 : C::kTQ0);
         const uint32_t tO = tmem + (t ? C::kO1 : C::kO0);
         const int halves = dump ? min(2 * n, 2) : 2 * n;
         // S_t[g % 2] = Q_t K^T over the 64 keys of half chunk g
@@ -434,18 +493,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((g & 1) == 0) {
             if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
             ptx::tc_fence_after();
-            if (t == 0) trace(p, kTrFullSeen, c);
+            if (t == 0) trace<kDiag>(p, kTrFullSeen, c);
           }
           const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep + uint32_t(g & 1) * kHalfRows;
           const uint32_t tS = tmem + s_col(t, g & 1);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
-            if (k == 0) ptx::mma_ss_lh<0>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
-            else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
+            if constexpr (C::kQTmem) {
+              // A = Q_t from TMEM: a k-step is 16 dims, 8 columns of bf16 pairs
+              ptx::mma_ts_lh(tS, tQ + 8 * k, k_lo + off, hi, idesc_qk, k > 0 ? 1u : 0u);
+            } else {
+              if (k == 0) ptx::mma_ss_lh<0>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
+              else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
+            }
           }
           ptx::mma_commit(s_full(t, g & 1));
-          trace(p, t ? kTrQk1 : ((g & 1) ? kTrQk0h1 : kTrQk0), c);
+          trace<kDiag>(p, t ? kTrQk1 : ((g & 1) ? kTrQk0h1 : kTrQk0), c);
           return true;
         };
         for (int g = 0; ok && g < min(halves, 2); ++g) ok = issue_qk(g);
@@ -453,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = g & 1, c = g >> 1, st = c % S;
           if (!(ok = ptx::mbar_wait_bounded(p_ready(t, b), c & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
-          trace(p, t ? kTrP1Seen : (b ? kTrP0h1Seen : kTrP0Seen), c);
+          trace<kDiag>(p, t ? kTrP1Seen : (b ? kTrP0h1Seen : kTrP0Seen), c);
           // O_t (+)= P V over the half's 64 keys: a k-step is 16 key rows (2 KB) of V and
           // 8 TMEM columns of packed P
           const uint32_t v_lo = v_lo_of(st) + uint32_t(b) * kHalfRows;
@@ -464,52 +528,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit(pv_done(t));
           if (b) {
             ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
-            if (t == 0) trace(p, kTrEmpty, c);
+            if (t == 0) trace<kDiag>(p, kTrEmpty, c);
           }
           if (g + 2 < halves) ok = issue_qk(g + 2);  // into the buffer the PV above reads (in order)
         }
       } else {
-        // Tail: S2^T = K Q2^T (M = 128 keys, N = 16 tail rows, K = 64), then
-        // O2 (+)= P2 V (M = 64, N = 64, K = 128 keys) with P2 from shared memory.  With
-        // M = 64 the accumulator's rows 16q..16q+15 live in TMEM lanes 32q..32q+15, so
-        // P2 row 16q + r (key group q, tail row r) lands in tail warp q's lane r.
+        // Tail: S2^T = K Q2^T (M = 128 keys, N = 16, K = 64) into one TMEM buffer, then
+        // O2^T (+)= V^T P2^T (M = 64 columns of V, N = 8 tail rows, K = 128 keys): A = V^T
+        // read MN-major from the V tile, B = P2^T K-major from shared memory.  With
+        // M = 64 the accumulator's rows (V columns) 16q..16q+15 live in TMEM lanes
+        // 32q..32q+15.
         constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailN, 0, 0);
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(64, 64, 0, 1);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(64, kTailMaxRows, 1, 0);
         const uint32_t q2_lo = uint32_t(ptx::smem_desc_sw128(sQ2, 16, 1024));
         const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
         const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
         const int nmma = dump ? 0 : n;
-        // S2^T[c % 2] = K_c Q2^T, issued one chunk ahead: before waiting for P2 of chunk c-1
-        // (its buffer was read by the softmax of chunk c-2, whose PV precedes it)
         auto issue_st = [&](int c) -> bool {
           const int st = c % S;
           if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
           ptx::tc_fence_after();
           const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
-          const uint32_t d = tS2 + uint32_t(kTailN * (c & 1));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            if (k == 0) ptx::mma_ss_lh<0>(d, k_lo, q2_lo, hi, idesc_st);
-            else ptx::mma_ss_lh<1>(d, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
+            if (k == 0) ptx::mma_ss_lh<0>(tS2, k_lo, q2_lo, hi, idesc_st);
+            else ptx::mma_ss_lh<1>(tS2, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
           }
-          ptx::mma_commit(s2_full(c & 1));
-          trace(p, kTrQk2, c);
+          ptx::mma_commit(s2_full);
+          trace<kDiag>(p, kTrQk2, c);
           return true;
         };
-        if (nmma > 0) ok = issue_st(0);
+        if (nmma > 0 && ok) ok = issue_st(0);
         for (int c = 0; ok && c < nmma; ++c) {
           const int st = c % S;
-          if (c + 1 < nmma && !(ok = issue_st(c + 1))) break;
+          if (c + 1 < nmma) {
+            // the single S2^T buffer is free once the tail warps have loaded chunk c's scores
+            if (!(ok = ptx::mbar_wait_bounded(s2_free, c & 1, limit, abort_flag))) break;
+            ptx::tc_fence_after();
+            if (!(ok = issue_st(c + 1))) break;
+          }
           if (!(ok = ptx::mbar_wait_bounded(p2_ready(c & 1), (c >> 1) & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
-          trace(p, kTrP2Seen, c);
+          trace<kDiag>(p, kTrP2Seen, c);
           const uint32_t v_lo = v_lo_of(st);
-          const uint32_t a_lo = p2_lo + uint32_t((c & 1) * (C::kP2Bytes >> 4));
+          const uint32_t b_lo = p2_lo + uint32_t((c & 1) * (kP2Bytes >> 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t off = uint32_t((k >> 2) * (kP2ColBlockBytes >> 4) + (k & 3) * 2);
-            if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
-            else ptx::mma_ss_lh<1>(tO2, a_lo + off, v_lo + uint32_t(128 * k), hi, idesc_pv);
+            const uint32_t boff = uint32_t((k >> 2) * (1024 >> 4) + (k & 3) * 2);
+            if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, v_lo, b_lo, hi, idesc_pv);
+            else ptx::mma_ss_lh<1>(tO2, v_lo + uint32_t(128 * k), b_lo + boff, hi, idesc_pv);
           }
           ptx::mma_commit(pv2_done);
           ptx::mma_commit(empty_bar(st));
@@ -533,10 +600,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS0 = tmem + s_col(t, 0) + lane_off;  // buffer b at + 64 b
     const uint32_t tO = tmem + (t ? C::kO1 : C::kO0) + lane_off;
     const int64_t qrow = int64_t(work.stream) * p.T + row;
-    if (tile_on)
-      store_q_row<D>(t ? sQ1 : sQ0, r,
-                     reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D),
-                     row_ok);
+    const uint4* qsrc =
+        reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D);
+    if (tile_on) {
+      if constexpr (C::kQTmem) {
+        // this row of Q into TMEM lane r: column j holds dims 2j (low half) and 2j + 1
+        uint32_t qv[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = row_ok ? __ldg(qsrc + c) : make_uint4(0, 0, 0, 0);
+          qv[4 * c] = v.x;
+          qv[4 * c + 1] = v.y;
+          qv[4 * c + 2] = v.z;
+          qv[4 * c + 3] = v.w;
+        }
+        ptx::tmem_st32(tmem + (t ? C::kTQ1 : C::kTQ0) + lane_off, qv);
+        ptx::tmem_wait_st();
+      } else {
+        store_q_row<D>(t ? sQ1 : sQ0, r, qsrc, row_ok);
+      }
+    }
     if constexpr (C::kOnes) {  // the ones block: 16 KB over the 256 main-softmax threads
       const uint32_t ones = 0x3F803F80u;  // two bf16 1.0
 #pragma unroll
@@ -546,23 +629,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
     }
     ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
     ptx::mbar_arrive(q_full);
 
     if (tile_on && dump) {
-      float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
-      for (int b = 0; b < 2 && n > 0; ++b) {
-        if (!ptx::mbar_wait_warp(s_full(t, b), 0, limit, abort_flag)) break;
-        ptx::tc_fence_after();
-        for (int j = 0; j < 2; ++j) {
-          uint32_t s[32];
-          ptx::tmem_ld32(tS0 + kHalfKeys * b + 32 * j, s);
-          ptx::tmem_wait_ld();
-          for (int e = 0; e < 32; ++e) dst[kHalfKeys * b + 32 * j + e] = __uint_as_float(s[e]);
+      if constexpr (kDiag) {
+        float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
+        for (int b = 0; b < 2 && n > 0; ++b) {
+          if (!ptx::mbar_wait_warp(s_full(t, b), 0, limit, abort_flag)) break;
+          ptx::tc_fence_after();
+          for (int j = 0; j < 2; ++j) {
+            uint32_t s[32];
+            ptx::tmem_ld32(tS0 + kHalfKeys * b + 32 * j, s);
+            ptx::tmem_wait_ld();
+            for (int e = 0; e < 32; ++e) dst[kHalfKeys * b + 32 * j + e] = __uint_as_float(s[e]);
+          }
         }
       }
     } else if (tile_on) {
       float m = -INFINITY;  // running max of scaled logits (log2 units)
-      float l = 0.f;        // running sum of the bf16-rounded P (without the ones block)
+      float l = 0.f;        // D = 128: running sum of the bf16-rounded P (D = 64 takes it from O)
       bool ok = true;
       int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
@@ -587,32 +673,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = ptx::mbar_wait_warp(s_full(t, b), (g >> 1) & 1, limit, abort_flag))) break;
         ptx::tc_fence_after();
-        if (q4 == 0 && lane == 0) trace(p, t ? kTrS1Seen : (b ? kTrS0h1Seen : kTrS0Seen), g >> 1);
+        if (q4 == 0 && lane == 0) trace<kDiag>(p, t ? kTrS1Seen : (b ? kTrS0h1Seen : kTrS0Seen), g >> 1);
         if (warp_on) {
-          // The half's 64 scores are exponentiated against the running max m while
-          // their own max is taken; only when a score exceeds m by more than 2^8 (in
-          // practice: the first half, and rare jumps) does the warp take the out-of-line
-          // path that moves m, rescales O and recomputes this half's P.  P (packed
-          // bf16 pairs) overwrites the first 32 columns of the half's S buffer.
+          // The half's 64 scores are exponentiated against the running max m; only when
+          // some P value reaches 2 (a rare jump of the max) does the warp take the
+          // out-of-line path that moves m, rescales O and recomputes this half's P.
+          // P (packed bf16 pairs) overwrites the first 32 columns of the half's S buffer.
           const uint32_t tS = tS0 + kHalfKeys * b;
-          uint32_t sa[32], sb[32], pk[32];
+          uint32_t sa[32], sb[32], pk[32], orr;
           ptx::tmem_ld32(tS, sa);
           ptx::tmem_ld32(tS + 32, sb);
           ptx::tmem_wait_ld();
           mask32(sa, kHalfKeys * b, len);
           mask32(sb, kHalfKeys * b + 32, len);
-          const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
-          const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk);
-          const bool need = mx > m + C::kThreshold;
+          const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk, &orr);
+          const bool need = (orr & kPHighBits) != 0;
           if (__any_sync(0xffffffffu, need)) {
-            const float m_new = need ? mx : m;
-            const float corr = need ? ptx::ex2(m - m_new) : 1.f;  // 0 while m is -inf
-            const float2 r2 = move_running_max<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, corr, -m_new, sl2,
-                                                           kHalfKeys * b, len, pv_done(t), uint32_t(g - 1) & 1u,
-                                                           limit, abort_flag);
-            if constexpr (!C::kOnes) l = l * corr + r2.x;
-            m = m_new;
-            if (r2.y == 0.f) {
+            const float4 r4 = move_running_max<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, need, m, sl2, kHalfKeys * b,
+                                                           len, pv_done(t), uint32_t(g - 1) & 1u, limit, abort_flag);
+            if constexpr (!C::kOnes) l = l * r4.z + r4.y;
+            m = r4.x;
+            if (r4.w == 0.f) {
               ok = false;
               break;
             }
@@ -622,11 +703,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_st();
           }
         }
+        if (len < kHalfKeys * (b + 1)) {
+          // ragged chunk: zero this half's V rows past the valid keys before the PV reads them
+          zero_v_rows<D>(sV((g >> 1) % S), max(len, kHalfKeys * b), kHalfKeys * (b + 1), r, 128);
+          ptx::fence_proxy_async_smem();
+        }
         ptx::tc_fence_before();
         // an arrive releases this thread's earlier writes, so the trace store follows it
-        const long long t_arrive = clock64();
+        long long t_arrive = 0;
+        if constexpr (kDiag) t_arrive = clock64();
         ptx::mbar_arrive(p_ready(t, b));
-        if (q4 == 0 && lane == 0) trace_at(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1, t_arrive);
+        if (q4 == 0 && lane == 0)
+          trace_at<kDiag>(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1, t_arrive);
       }
       if (!ok) signal_abort(p.status, abort_flag);
       if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
@@ -653,18 +741,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_arrive(q_full);
   } else {
     // ------------------------------------------------------------ tail softmax (warps 0-3)
-    const int q = warp;  // TMEM lane quarter = key group [32q, 32q+32) of each chunk
+    const int q = warp;  // key group [32q, 32q+32) of each chunk; TMEM lane quarter q
+    const int tid = q * 32 + lane;
     const int tail_rows = p.tail_rows;
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const uint32_t tS2 = tmem + C::kS2 + lane_off;
     const uint32_t tO2 = tmem + C::kO2 + lane_off;
+    // exchange area: [2][4 warps][8 rows] maxima, then [2][4 warps] "waits succeeded" flags
+    float* xmax = reinterpret_cast<float*>(smem + C::kTailX);
+    int* xok = reinterpret_cast<int*>(xmax + 2 * 4 * kTailMaxRows);
     if (has_tail) {
-      // zero both P tiles (entries off the diagonal key-group blocks stay zero), then
-      // stage the tail's Q rows (rows past tail_rows are zero) as the MMA's B operand
-      const int idx = q * 32 + lane;
-#pragma unroll
-      for (int i = 0; i < 2 * C::kP2Bytes / (128 * 16); ++i) st_shared_zero16(sP2 + uint32_t((i * 128 + idx) * 16));
-      const int qr = idx >> 3, qc = idx & 7;
+      // zero both P tiles (rows past tail_rows stay zero), then stage the tail's Q rows
+      // (rows past tail_rows are zero) as the B operand of S2^T
+      for (int i = tid; i < 2 * kP2Bytes / 16; i += 128) st_shared_zero16(sP2 + uint32_t(i * 16));
+      const int qr = tid >> 3, qc = tid & 7;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (qr < tail_rows) {
         const int64_t qrow = int64_t(work.stream) * p.T + tail_row0 + qr;
@@ -679,147 +769,139 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(q_full);
     if (has_tail && !dump) {
-      // per row r: m[r] warp-uniform running max (log2 units) of this key group,
-      // l[r] this lane's share of the row sum of the rounded P
+      // per row r: m[r] the running max (log2 units; the same in all four warps), l[r]
+      // this lane's share of the row sum of the rounded P
       float m[kTailMaxRows], l[kTailMaxRows];
 #pragma unroll
       for (int rr = 0; rr < kTailMaxRows; ++rr) {
         m[rr] = -INFINITY;
         l[rr] = 0.f;
       }
+      // Every tail thread passes the same barriers in every chunk, whatever its waits
+      // returned, so no warp can be left waiting at a barrier another one skipped; a
+      // failed wait ends the loop of all four warps at the next exchange.
       bool ok = true;
       const int key = 32 * q + lane;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
-      for (int j = 0; ok && j < n; ++j) {
+      for (int j = 0; j < n; ++j) {
         const int len = len_next;
         if (j + 1 < n) len_next = __ldg(&p.chunks[c0 + j + 1].start_len) >> 16;
-        if (!(ok = ptx::mbar_wait_warp(s2_full(j & 1), (j >> 1) & 1, limit, abort_flag))) break;
-        ptx::tc_fence_after();
-        if (q == 0 && lane == 0) trace(p, kTrS2Seen, j);
-        uint32_t s[16];
-        ptx::tmem_ld16(tS2 + uint32_t(kTailN * (j & 1)), s);
-        ptx::tmem_wait_ld();
-        // The row offsets m[r] are only refreshed (an exact warp max) when some lane's
-        // score exceeds them by more than 2^8, so the common chunk needs no reduction.
-        const bool valid = key < len;
+        const bool okj = ok && ptx::mbar_wait_warp(s2_full, j & 1, limit, abort_flag);
         float xs[kTailMaxRows];
-        uint32_t need = 0;
-#pragma unroll
-        for (int rr = 0; rr < kTailMaxRows; ++rr) {
-          xs[rr] = valid ? __uint_as_float(s[rr]) * sl2 : -INFINITY;
-          if (rr < tail_rows && xs[rr] > m[rr] + kRescaleThreshold) need |= 1u << rr;
-        }
-        const uint32_t rows_moved = __reduce_or_sync(0xffffffffu, need);
-        if (rows_moved) {
-          float my_corr = 1.f;  // factor for the O2 row held by this lane (lane = tail row)
+        bool need = false;
+        if (okj) {
+          ptx::tc_fence_after();
+          if (q == 0 && lane == 0) trace<kDiag>(p, kTrS2Seen, j);
+          uint32_t s[16];
+          ptx::tmem_ld16(tS2, s);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(s2_free);  // the issuer may now write the next chunk's S2^T
+          const bool valid = key < len;
 #pragma unroll
           for (int rr = 0; rr < kTailMaxRows; ++rr) {
-            if ((rows_moved >> rr) & 1u) {
-              const float mx = warp_max(xs[rr]);
-              const float corr = ptx::ex2(m[rr] - mx);  // 0 while m is -inf
-              l[rr] *= corr;
-              if (lane == rr) my_corr = corr;
-              m[rr] = mx;
-            }
+            xs[rr] = valid ? __uint_as_float(s[rr]) * sl2 : -INFINITY;
+            if (rr < tail_rows && xs[rr] > m[rr] + kThreshold) need = true;
           }
-          if (j > 0) {  // O2 must first hold the previous chunk's PV
+        } else {
+#pragma unroll
+          for (int rr = 0; rr < kTailMaxRows; ++rr) xs[rr] = -INFINITY;
+        }
+        if (tail_bar_or(need || !okj)) {
+          // rare: a running max moves (or a wait failed): each warp's maxima and status
+          // through shared memory, double-buffered by chunk parity
+          float* xm = xmax + (j & 1) * 4 * kTailMaxRows;
+#pragma unroll
+          for (int rr = 0; rr < kTailMaxRows; ++rr) {
+            const float wm = warp_max(xs[rr]);
+            if (lane == rr) xm[q * kTailMaxRows + rr] = wm;
+          }
+          if (lane == 0) xok[(j & 1) * 4 + q] = okj ? 1 : 0;
+          tail_bar_sync();
+          if (!(xok[(j & 1) * 4] && xok[(j & 1) * 4 + 1] && xok[(j & 1) * 4 + 2] && xok[(j & 1) * 4 + 3])) {
+            ok = false;
+            break;  // all four warps read the same flags and leave together
+          }
+          float corr[kTailMaxRows];
+#pragma unroll
+          for (int rr = 0; rr < kTailMaxRows; ++rr) {
+            float mx = m[rr];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) mx = fmaxf(mx, xm[g * kTailMaxRows + rr]);
+            corr[rr] = mx == m[rr] ? 1.f : ptx::ex2(m[rr] - mx);  // 0 while m is -inf
+            l[rr] *= corr[rr];
+            m[rr] = mx;
+          }
+          if (j > 0) {  // O2^T must first hold the previous chunk's PV
             if (!ptx::mbar_wait_warp(pv2_done, uint32_t(j - 1) & 1u, limit, abort_flag)) {
-              ok = false;
-              break;
+              ok = false;  // reported at the next chunk's exchange (or after the loop)
+              continue;
             }
             ptx::tc_fence_after();
-            rescale_tmem(tO2, 64, my_corr);
+            uint32_t o[8];
+            ptx::tmem_ld8(tO2, o);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int rr = 0; rr < kTailMaxRows; ++rr) o[rr] = __float_as_uint(__uint_as_float(o[rr]) * corr[rr]);
+            ptx::tmem_st8(tO2, o);
             ptx::tmem_wait_st();
           }
         }
+        const uint32_t p2 = sP2 + uint32_t((j & 1) * kP2Bytes);
 #pragma unroll
         for (int rr = 0; rr < kTailMaxRows; ++rr) {
           if (rr < tail_rows) {
-            const float neg_m = (m[rr] == -INFINITY) ? 0.f : -m[rr];  // no key seen yet: p = 0
-            const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs[rr] + neg_m));
+            const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs[rr] - m[rr]));
             l[rr] += __bfloat162float(pb);
-            st_shared_u16(p2_addr(sP2 + uint32_t((j & 1) * C::kP2Bytes), 16 * q + rr, key), __bfloat16_as_ushort(pb));
+            st_shared_u16(p2_addr(p2, rr, key), __bfloat16_as_ushort(pb));
           }
         }
-        ptx::fence_proxy_async_smem();  // P2 stores -> visible to the tensor core
+        if (len < kChunkTokens) zero_v_rows<D>(sV(j % S), len, kChunkTokens, tid, 128);
+        ptx::fence_proxy_async_smem();  // P2 stores (and zeroed V rows) -> visible to the tensor core
         ptx::tc_fence_before();
-        const long long t_arrive = clock64();
+        long long t_arrive = 0;
+        if constexpr (kDiag) t_arrive = clock64();
         ptx::mbar_arrive(p2_ready(j & 1));
-        if (q == 0 && lane == 0) trace_at(p, kTrP2Arrive, j, t_arrive);
+        if (q == 0 && lane == 0) trace_at<kDiag>(p, kTrP2Arrive, j, t_arrive);
       }
       if (!ok) signal_abort(p.status, abort_flag);
-      // this key group's (max, sum) of tail row `lane`
-      float my_m = -INFINITY, my_l = 0.f;
-#pragma unroll
-      for (int rr = 0; rr < kTailMaxRows; ++rr) {
-        if (rr < tail_rows) {
-          const float lt = warp_sum(l[rr]);
-          if (lane == rr) {
-            my_m = m[rr];
-            my_l = lt;
-          }
-        }
-      }
-      // merge the four key-group partial states of every tail row
-      // The merge scratch reuses the K/V stage ring, so it may be written only once every
+      // Row sums over all 128 keys of every chunk: each warp's share through shared
+      // memory.  The exchange reuses the K/V stage ring, so it is written only once every
       // consumer's MMAs (and with them every load of this CTA) have completed.
       float* scratch = reinterpret_cast<float*>(smem + C::kKV);
-      float* sm = scratch + 4 * kTailMaxRows * 64;
-      float* sl = sm + 4 * kTailMaxRows;
       bool done = ok;
       for (int u = 0; u < 3 && done; ++u)
         if (u == 2 || u < n_main) done = ptx::mbar_wait_warp(o_done(u), 0, limit, abort_flag);
       if (done) {
-        ptx::tc_fence_after();
-        if (lane < tail_rows) {
-          sm[q * kTailMaxRows + lane] = my_m;
-          sl[q * kTailMaxRows + lane] = my_l;
-        }
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tO2 + 32 * j, v);
-          ptx::tmem_wait_ld();
-          if (lane < tail_rows) {
-            float4* dst = reinterpret_cast<float4*>(scratch + (q * kTailMaxRows + lane) * 64 + 32 * j);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                   __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
-          }
+        for (int rr = 0; rr < kTailMaxRows; ++rr) {
+          const float lt = warp_sum(l[rr]);
+          if (lane == 0) scratch[q * kTailMaxRows + rr] = lt;
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      tail_bar_sync();
       if (done && !*abort_flag) {
-        for (int rr = q; rr < tail_rows; rr += 4) {
-          float mm = -INFINITY;
+        ptx::tc_fence_after();
+        uint32_t o[8];
+        ptx::tmem_ld8(tO2, o);  // lane i < 16 of quarter q: column 16q + i of V, the 8 rows
+        ptx::tmem_wait_ld();
+        if (lane < 16) {
+          const int d = 16 * q + lane;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) mm = fmaxf(mm, sm[g * kTailMaxRows + rr]);
-          float w[4], L = 0.f;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            // a key group that saw no valid key has m = -inf and contributes nothing
-            w[g] = sm[g * kTailMaxRows + rr] == -INFINITY ? 0.f : exp2f(sm[g * kTailMaxRows + rr] - mm);
-            L += w[g] * sl[g * kTailMaxRows + rr];
-          }
-          float acc[2] = {0.f, 0.f};
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const float* src = scratch + (g * kTailMaxRows + rr) * 64 + 2 * lane;
-            acc[0] += w[g] * src[0];
-            acc[1] += w[g] * src[1];
-          }
-          const float inv = 1.f / L;
-          const int orow = tail_row0 + rr;
-          if (work.nsplit == 1) {
-            const int64_t qr = int64_t(work.stream) * p.T + orow;
-            uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + (qr * p.H + head) * D);
-            dst[lane] = pack_bf16(acc[0] * inv, acc[1] * inv);
-          } else {
-            const int64_t idx = (int64_t(split) * p.H + head) * p.T + orow;
-            *reinterpret_cast<float2*>(p.part_o + part_o_offset<D>(split, head, orow, 2 * lane, p.H, p.T)) =
-                make_float2(acc[0] * inv, acc[1] * inv);
-            if (lane == 0) p.part_lse[idx] = mm + __log2f(L);
+          for (int rr = 0; rr < kTailMaxRows; ++rr) {
+            if (rr < tail_rows) {
+              const float L = (scratch[rr] + scratch[kTailMaxRows + rr]) +
+                              (scratch[2 * kTailMaxRows + rr] + scratch[3 * kTailMaxRows + rr]);
+              const float val = __uint_as_float(o[rr]) / L;
+              const int orow = tail_row0 + rr;
+              if (work.nsplit == 1) {
+                const int64_t qr = int64_t(work.stream) * p.T + orow;
+                static_cast<__nv_bfloat16*>(p.out)[(qr * p.H + head) * D + d] = __float2bfloat16_rn(val);
+              } else {
+                p.part_o[part_o_offset<D>(split, head, orow, d, p.H, p.T)] = val;
+                if (d == 0) p.part_lse[(int64_t(split) * p.H + head) * p.T + orow] = m[rr] + __log2f(L);
+              }
+            }
           }
         }
       }
@@ -834,9 +916,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kDiag>
 cudaError_t configure_tc() {
-  return cudaFuncSetAttribute(attention_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kLaunch);
+  return cudaFuncSetAttribute(attention_tc_kernel<D, kDiag>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<D>::kLaunch);
 }
 
 template <int D>
@@ -844,15 +927,21 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t 
   constexpr int smem = Cfg<D>::kLaunch;
   const int64_t grid = int64_t(p.num_splits) * p.H * p.ngroups;
   if (grid <= 0 || grid > 0x7fffffff) return cudaErrorInvalidValue;
-  attention_tc_kernel<D><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
+  if (p.trace != nullptr || p.dump_scores != nullptr)
+    attention_tc_kernel<D, true><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
+  else
+    attention_tc_kernel<D, false><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t configure_attention_bf16() {
-  cudaError_t e = configure_tc<64>();
-  return e != cudaSuccess ? e : configure_tc<128>();
+  cudaError_t e;
+  if ((e = configure_tc<64, false>()) != cudaSuccess) return e;
+  if ((e = configure_tc<64, true>()) != cudaSuccess) return e;
+  if ((e = configure_tc<128, false>()) != cudaSuccess) return e;
+  return configure_tc<128, true>();
 }
 
 cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s) {
