@@ -94,6 +94,17 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def fp32_alu_peak_tflops() -> float:
+    """fp32 FMA peak of the CUDA cores: SMs x 128 FMA lanes x 2 FLOP x maximum SM clock
+    (the clock from MEASURED_PEAKS.json, else the GB300's 2070 MHz)."""
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            mhz = float(json.load(fh).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def visible_tokens(w: wl.Workload, f: int) -> int:
     """Visible keys per stream after f frames: (min(f,sc) + min(max(f-sc,0),w)) * P + f * S."""
     sc, win, P, S = w.scale_frames, w.sliding_window, w.patches_per_frame, w.specials_per_frame
@@ -521,12 +532,15 @@ def run_gpu(args, w: wl.Workload):
     flops = statistics.mean(block_work(w, x)[0] for x in frames_timed)
     byts = statistics.mean(block_work(w, x)[1] for x in frames_timed)
     avg_launch = statistics.mean(launch_ms) / 1000.0
-    t_roof_block = max(flops / (tflops * 1e12), byts / (hbm * 1e9))
-    bound = "hbm" if byts / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor"
+    compute_peak, compute_bound, compute_src = tflops, "tensor", "bf16_tflops"
+    if w.dtype == "f32":  # the fp32 path runs on the CUDA cores' FMA units
+        compute_peak, compute_bound, compute_src = fp32_alu_peak_tflops(), "alu", "fp32 FMA: 152 SMs x 128 lanes x 2 x max SM clock"
+    t_roof_block = max(flops / (compute_peak * 1e12), byts / (hbm * 1e9))
+    bound = "hbm" if byts / (hbm * 1e9) >= flops / (compute_peak * 1e12) else compute_bound
     if bound == "hbm":
         achieved, peak, unit = byts / avg_launch / 1e9, hbm, "GB/s"
     else:
-        achieved, peak, unit = flops / avg_launch / 1e12, tflops, "TFLOP/s"
+        achieved, peak, unit = flops / avg_launch / 1e12, compute_peak, "TFLOP/s"
     value = aggregate_throughput(K, world, max_elapsed)
     step_ms = max_elapsed / K * 1000.0
     launches_per_step = B * L + L + (L if info["merge_needed"] else 0)
@@ -536,15 +550,19 @@ def run_gpu(args, w: wl.Workload):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": w.dtype, "data": "synthetic",
         "config": {**workload_config(w, f_first + K), "timed_frames": [f_first + 1, f_first + K],
                    **({"rope": {"sections": list(sections), "theta": theta}} if args.rope else {}),
                    "l2": "no flush: visible K/V per block exceeds L2",
                    "parallelism": f"replicas x{world} (independent streams, no data-path collective)"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                     "kernel": "attention (tcgen05 paged attention + LSE merge), per block launch",
-                     "peak_source": f"{peak_kind} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+                     "kernel": ("attention (fp32 CUDA-core paged attention + LSE merge), per block launch"
+                                if w.dtype == "f32" else
+                                "attention (tcgen05 paged attention + LSE merge), per block launch"),
+                     "peak_source": (f"{peak_kind} (hbm_gbs)" if bound == "hbm" else
+                                     "derived (" + compute_src + ")" if bound == "alu" else
+                                     f"{peak_kind} (bf16_tflops)"),
                      "avg_launch_us": avg_launch * 1e6, "algorithmic_bytes_per_launch": byts,
                      "algorithmic_flops_per_launch": flops,
                      "tensor_tflops": flops / avg_launch / 1e12, "hbm_gbs": byts / avg_launch / 1e9},
@@ -696,6 +714,8 @@ def main(argv=None):
                     help="tuning only: force this many KV splits per stream (0 = the planner's choice)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="profiling only: override the block count (smaller device footprint)")
+    ap.add_argument("--f32", action="store_true",
+                    help="the workload stored in fp32 and attended by the fp32 accuracy path")
     ap.add_argument("--query-frames", type=int, default=1,
                     help="F > 1: time the scale-phase prefill (F frames appended, then F*T query rows "
                          "attend over them) instead of the streaming step")
@@ -703,6 +723,8 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "spk":
         args.warmup = 3
     w = wl.CONFIGS[args.workload]
+    if args.f32:
+        w = w.replace(dtype="f32", name=f"{w.name}_f32")
     if args.blocks:
         w = w.replace(num_blocks=args.blocks, name=f"{w.name}_blocks{args.blocks}")
     if args.impl == "reference":

@@ -31,13 +31,16 @@ int spk_debug_dump_scores(spk_cache* cache, int block, const void* q, float* dst
 /* Diagnostics for the bf16 tensor-core kernel: run block's attention exactly as
  * spk_run_attention does (same outputs) while the first CTA records the SM clock
  * (clock64) of its pipeline events for each of its first `capacity` chunks into
- * trace[event][chunk] (device memory, 20 * capacity uint64).  Events, in order:
+ * trace[event][chunk] (device memory, 20 * capacity + 2 uint64).  Events, in order:
  * TMA issue, MMA (tile 0) sees K/V landed, S0 keys 0..63 issued, its P seen, S1 keys
  * 0..63 issued, its P seen, tail S^T issued, tail P seen, S0 keys 64..127 issued, its
  * P seen, K/V stage released by tile 0, softmax 0 sees S (keys 0..63), softmax 0
  * signals P, softmax 1 sees S (keys 0..63), softmax 1 signals P, tail sees S^T, tail
  * signals P, softmax 0 sees S (keys 64..127), softmax 0 signals P, K/V landed in
- * shared memory.  Entries of events that do not happen are left as they were. */
+ * shared memory.  Entries of events that do not happen are left as they were.  The two
+ * words after the 20 * capacity event clocks count, over every CTA of the launch, the
+ * times a running max moved after O had started to accumulate (so O was rescaled): by
+ * a main-tile softmax warp, and by the tail warps; the call adds to what they hold. */
 int spk_debug_trace_attention(spk_cache* cache, int block, const void* q, void* out, void* workspace,
                               uint64_t* trace, int32_t capacity, void* cuda_stream);
 

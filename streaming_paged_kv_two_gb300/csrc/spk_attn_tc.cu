@@ -12,39 +12,46 @@
 // Reconstruction Over SDPA", "Efficient Attention Masking and Padding").
 //
 // One CTA (one per SM) = (KV split, head, query-row group).  A group is up to two
-// 128-row "main" tiles, plus, on the last group when head_dim is 64, a "tail" of at
-// most 8 trailing rows (262 = 2 x 128 + 6).  Warp roles (16 warps):
+// 128-row "main" tiles, plus, on the last group, a "tail" of at most 8 trailing rows
+// (262 = 2 x 128 + 6).  Keys are processed in 64-key halves of the 128-key chunks.
+// Warp roles (16 warps):
 //   warps 4-7   softmax of main tile 0, warps 8-11 softmax of main tile 1: one
-//               thread per query row (= TMEM lane).  Each tile has two 64-key score
-//               buffers in TMEM, so Q K^T of the next half chunk runs on the tensor
-//               core while the softmax works on the current one.  fp32 online
-//               softmax in log2 units: a half's scores are exponentiated against the
-//               running max m and the packed bf16 P words are OR-ed together; only
-//               when one of them reaches 2.0 (a score more than 1 above m) does the
-//               warp move m, rescale O in TMEM and recompute the half.  Masking of
-//               the chunk's ragged tail; P written back as bf16 over S.
+//               thread per query row (= TMEM lane).  fp32 online softmax in log2 units:
+//               a half's scores are exponentiated against the running max m and the
+//               packed bf16 P words OR-ed together; only when one of them reaches 2.0 (a
+//               score more than 1 above m) does the warp move m, rescale O in TMEM and
+//               recompute the half; masking of the chunk's ragged tail.  Two schedules:
+//               head_dim 64: each tile has two 64-key S buffers, so Q K^T of the next
+//               half runs while the softmax works on the current one, and P is written
+//               back over S (measured faster for D = 64);
+//               head_dim 128: one S buffer per tile, released as soon as the softmax
+//               has loaded its scores into registers (the next Q K^T then overlaps the
+//               exponentials), and P goes to the tile's own P buffer once the previous
+//               half's PV has read it; this frees the TMEM for the tail.
 //   warps 0-3   tail softmax.  The tail is computed transposed: S2^T = K Q2^T
 //               (M = 128 keys, N = 16 rows), so a thread holds one key's scores for
 //               every tail row; warp q owns keys [32q, 32q+32) of each chunk.  The four
 //               warps share one running max per row (moved, rarely, after a barrier
 //               that ORs their "score above the max" flags), so one
-//               O2^T += V^T P2^T (M = 64 columns of V, N = 8 rows, K = 128 keys, P2
+//               O2^T += V^T P2^T (M = D columns of V, N = 8 or 16 rows, K = 128 keys, P2
 //               from shared memory) accumulates a whole chunk.
 //   warp 12     TMA producer: K and V chunk tiles gathered by page id through a
 //               4-D tensor map over the pool (d, head, token, 2*page+kv), 128-byte
 //               swizzle, into a ring of shared-memory stages.
 //   warps 13-15 MMA issuers, one thread per consumer (main tile 0, main tile 1,
-//               tail).  Main tile t, half chunk g: S_t[g%2] = Q_t K_g^T (M=128, N=64,
-//               K=D), then, once the softmax has written P_g, O_t += P_g V_g (M=128,
-//               N=D, K=64) followed by Q K^T of half g+2 into the buffer just read.
-//               The consumers advance independently; a K/V stage is released once
-//               every consumer is done with it.
+//               tail).  Main tile t, half chunk g: S = Q_t K_g^T (M=128, N=64, K=D) and,
+//               once the softmax has written P_g, O_t += P_g V_g (M=128, N=D, K=64);
+//               head_dim 64 issues Q K^T of half g+2 into the buffer the PV just read,
+//               head_dim 128 issues Q K^T of half g+1 once the softmax has released
+//               the S buffer.  The consumers advance independently; a K/V stage is
+//               released once every consumer is done with it.
 // head_dim 64: Q_t is the TMEM A operand of Q K^T (only K is read from shared memory),
 // and the PV MMA's B operand is V extended by a 16-column block of ones in shared
 // memory, so O0/O1 are 80 columns wide and column 64 accumulates the row sum of the bf16
-// P that the MMA consumed.  TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each)
-// | O0 | O1 (80 each) | Q0 | Q1 (32 each) | S2^T (16) | O2^T (8).
-// head_dim 128: Q in shared memory; S (4 x 64) | O0 | O1 (128 each); fp32 row sums.
+// P that the MMA consumed.  TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) |
+// O0 | O1 (80 each) | Q0 | Q1 (32 each) | S2^T (16) | O2^T (8).
+// head_dim 128: Q in shared memory; S0 | S1 | P0 | P1 | O0 | O1 (128 each) | S2^T (16) |
+// O2^T (16); fp32 row sums.
 // Key rows past a ragged chunk's length are zeroed in the V tile before a PV MMA reads
 // them, so whatever a slot past the valid tokens holds (a rolled-back frame, an earlier
 // stream) cannot reach the output, not even as 0 * Inf.
@@ -63,9 +70,8 @@ namespace spk {
 namespace {
 
 constexpr int kColBlockBytes = 128 * 128;  // 128 rows x 64 bf16: one 128-byte-swizzled column block
-constexpr int kTailMaxRows = 8;            // rows of the tail (N of O2^T)
+constexpr int kTailMaxRows = 8;            // rows of the tail
 constexpr int kTailN = 16;                 // N of S2^T (M = 128 needs N >= 16)
-constexpr int kP2Bytes = kTailMaxRows * 256;  // one tail P tile: 8 rows x 128 keys bf16 (two 1 KB column blocks)
 constexpr int kHalfKeys = 64;              // keys per main-tile score buffer
 constexpr int kThreads = 512;
 constexpr int kWarpMain = 4;   // first warp of main tile 0; tile 1 starts at 8
@@ -82,42 +88,59 @@ constexpr int align1024(int x) { return (x + 1023) & ~1023; }
 template <int D>
 struct Cfg {
   static constexpr int kTile = 128 * D * 2;  // one Q, K or V tile in shared memory
-  static constexpr bool kTail = (D == 64);
+  static constexpr bool kTail = true;
+  // N of O2^T = V^T P2^T: 8 rows with M = 64 (D = 64); M = 128 needs N >= 16 (rows 8-15 zero)
+  static constexpr int kTailPvN = (D == 64) ? 8 : 16;
+  static constexpr int kP2ColBlock = kTailPvN * 128;  // one 64-key column block of a tail P tile
+  static constexpr int kP2Bytes = 2 * kP2ColBlock;    // one tail P tile: kTailPvN rows x 128 keys bf16
+  static constexpr int kQ2ColBlock = kTailN * 128;    // one 64-dim column block of the tail Q tile
   // D == 64: the row sums come out of the PV MMA, whose B operand is V extended by a
   // 16-column block of ones (O gets 16 more columns, each holding the row sum)
   static constexpr bool kOnes = (D == 64);
   // D == 64: Q lives in TMEM as the A operand of Q K^T
   static constexpr bool kQTmem = (D == 64);
+  // D == 128: one S buffer per tile, released once loaded, and a separate P buffer
+  static constexpr bool kEarly = (D == 128);
   static constexpr int kStages = (D == 64) ? 6 : 2;
   // shared memory
-  static constexpr int kQ0 = 0;          // D == 128: the two Q tiles
+  static constexpr int kQ0 = 0;                                   // D == 128: the two Q tiles
   static constexpr int kQ1 = kTile;
-  static constexpr int kQ2 = 0;          // D == 64: tail Q, 16 rows x 128 bytes
-  static constexpr int kP2 = 2048;       // D == 64: two tail P tiles
-  static constexpr int kKV = kTail ? align1024(kP2 + 2 * kP2Bytes) : 2 * kTile;
+  static constexpr int kQ2 = kQTmem ? 0 : 2 * kTile;              // tail Q: 16 rows, D/64 column blocks
+  static constexpr int kP2 = kQ2 + (D / 64) * kQ2ColBlock;         // two tail P tiles
+  static constexpr int kKV = align1024(kP2 + 2 * kP2Bytes);
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kOnesBlk = kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones (kOnes)
   static constexpr int kTailX = kOnesBlk + (kOnes ? kColBlockBytes : 0);  // tail exchange: [2][4][8] maxima, [2][4] flags
   static constexpr int kBars = kTailX + (kTail ? 2 * 4 * (kTailMaxRows + 1) * 4 + 32 : 0);
-  // full[S], empty[S], q_full, s_full[2][2], p_ready[2][2], pv_done[2], o_done[3], s2_full,
-  // s2_free, p2_ready[2], pv2_done
-  static constexpr int kNumBars = 2 * kStages + 19;
+  // full[S], empty[S], q_full, s_full[2][2], s_free[2], p_ready[2][2], pv_done[2], o_done[3],
+  // s2_full, s2_free, p2_ready[2], pv2_done
+  static constexpr int kNumBars = 2 * kStages + 21;
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kOW = D + (kOnes ? 16 : 0);  // TMEM columns of a main tile's O
-  static constexpr uint32_t kO0 = 4 * kHalfKeys, kO1 = 4 * kHalfKeys + kOW;
-  static constexpr uint32_t kTQ0 = kO1 + kOW, kTQ1 = kTQ0 + D / 2;   // D == 64: Q0, Q1 as bf16 pairs
-  static constexpr uint32_t kS2 = kTQ1 + D / 2, kO2 = kS2 + kTailN;  // D == 64: S2^T, O2^T
-  static_assert(kTail ? kO2 + kTailMaxRows <= 512 : kO1 + kOW <= 512, "TMEM budget");
-  static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kOnesBlk % 1024 == 0,
+  // D == 64: S_t[b] at 64 (2t + b), P over S; D == 128: S_t at 64 t, P_t at kP0 + 32 t
+  static constexpr uint32_t kP0 = 2 * kHalfKeys;
+  static constexpr uint32_t kO0 = kEarly ? kP0 + kHalfKeys : 4 * kHalfKeys, kO1 = kO0 + kOW;
+  static constexpr uint32_t kTQ0 = kO1 + kOW, kTQ1 = kTQ0 + (kQTmem ? D / 2 : 0);  // D == 64: Q0, Q1
+  static constexpr uint32_t kS2 = kTQ1 + (kQTmem ? D / 2 : 0), kO2 = kS2 + kTailN;  // S2^T, O2^T
+  static_assert(kO2 + kTailPvN <= 512, "TMEM budget");
+  static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kQ2 % 1024 == 0 && kOnesBlk % 1024 == 0 &&
+                kP2ColBlock % 1024 == 0 && kQ2ColBlock % 1024 == 0,
                 "128-byte-swizzled tiles start on 1024-byte boundaries");
-  static_assert(!kTail || kQ2 + 2048 <= kP2, "tail Q tile");
   static_assert(kLaunch <= 227 * 1024, "shared memory per CTA");
 };
 
-// TMEM column of main tile t's score buffer b
-__device__ __forceinline__ uint32_t s_col(int t, int b) { return uint32_t(kHalfKeys * (2 * t + b)); }
+
+// TMEM columns of main tile t's scores and P for half chunk b
+template <int D>
+__device__ __forceinline__ uint32_t s_col(int t, int b) {
+  return Cfg<D>::kEarly ? uint32_t(kHalfKeys * t) : uint32_t(kHalfKeys * (2 * t + b));
+}
+template <int D>
+__device__ __forceinline__ uint32_t p_col(int t, int b) {
+  return Cfg<D>::kEarly ? Cfg<D>::kP0 + uint32_t(kHalfKeys / 2 * t) : s_col<D>(t, b);
+}
 
 // Trace mode (diagnostics): CTA 0 records the SM clock of an event for a chunk.
 template <bool kDiag>
@@ -153,10 +176,11 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Byte address of element (row, key) of a tail P tile: 8 rows x 128 keys bf16, K-major,
-// 128-byte swizzle, keys 0-63 and 64-127 in two 1 KB column blocks.
-__device__ __forceinline__ uint32_t p2_addr(uint32_t base, int row, int key) {
-  return base + uint32_t((key >> 6) * 1024 + row * 128 + ((((key & 63) >> 3) ^ row) << 4) + (key & 7) * 2);
+// Byte address of element (row, key) of a tail P tile: rows x 128 keys bf16, K-major,
+// 128-byte swizzle, keys 0-63 and 64-127 in two column blocks of col_block bytes.
+__device__ __forceinline__ uint32_t p2_addr(uint32_t base, int col_block, int row, int key) {
+  return base + uint32_t((key >> 6) * col_block + (row >> 3) * 1024 + (row & 7) * 128 +
+                         ((((key & 63) >> 3) ^ (row & 7)) << 4) + (key & 7) * 2);
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
@@ -275,17 +299,20 @@ __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float co
   }
 }
 
-// Rare path of the online softmax (kept out of line so the hot loop's registers are
-// not spent on it), taken when some P value of the warp reached 2: every row that did
-// (`need`) moves its running max m to max(m, the half's max); O (every earlier PV of
-// this tile: when o_cols > 0, wait for the previous half's PV, tracked by pv_bar) is
-// scaled by corr = 2^(m - m_new), and the half's P is recomputed from S (still in TMEM)
-// with the new offset and stored over it.  Returns (m_new, sum of the new rounded P when
-// kSum, corr, 1 if the wait succeeded else 0).
+// Rare path of the online softmax, taken when some P value of the warp reached 2: every
+// row that did (`need`) moves its running max m to max(m, the half's max); O (every
+// earlier PV of this tile: when o_cols > 0, wait for the previous half's PV, tracked by
+// pv_bar) is scaled by corr = 2^(m - m_new), and the half's P is recomputed with the new
+// offset.  Returns (m_new, sum of the new rounded P when kSum, corr, 1 if the wait
+// succeeded else 0).
+//
+// head_dim 64: the scores are still in TMEM (the S buffer is not released before P is
+// stored over it), so this path reloads them and stores P itself; kept out of line so
+// the hot loop's registers are not spent on it.
 template <bool kSum>
-__device__ __noinline__ float4 move_running_max(uint32_t tO, uint32_t tS, int o_cols, bool need, float m, float sl2,
-                                                int first_key, int len, uint32_t pv_bar, uint32_t parity,
-                                                long long limit, const volatile int* abort_flag) {
+__device__ __noinline__ float4 move_running_max_tmem(uint32_t tO, uint32_t tS, int o_cols, bool need, float m,
+                                                     float sl2, int first_key, int len, uint32_t pv_bar,
+                                                     uint32_t parity, long long limit, const volatile int* abort_flag) {
   uint32_t sa[32], sb[32], pk[32], orr;
   ptx::tmem_ld32(tS, sa);
   ptx::tmem_ld32(tS + 32, sb);
@@ -294,7 +321,7 @@ __device__ __noinline__ float4 move_running_max(uint32_t tO, uint32_t tS, int o_
   mask32(sb, first_key + 32, len);
   const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
   const float m_new = need ? fmaxf(m, mx) : m;
-  const float corr = m_new == m ? 1.f : ptx::ex2(m - m_new);
+  const float corr = m_new == m ? 1.f : ptx::ex2(m - m_new);  // 0 while m is -inf
   bool ok = true;
   if (o_cols) {
     ok = ptx::mbar_wait_warp(pv_bar, parity, limit, abort_flag);
@@ -304,6 +331,28 @@ __device__ __noinline__ float4 move_running_max(uint32_t tO, uint32_t tS, int o_
   const float sum = exp_pack64<kSum>(sa, sb, sl2, -m_new, pk, &orr);
   ptx::tmem_st32(tS, pk);
   ptx::tmem_wait_st();
+  return make_float4(m_new, sum, corr, ok ? 1.f : 0.f);
+}
+
+// head_dim 128: the S buffer has been released, so the path works on the (masked)
+// scores held in registers and leaves the new P in pk; inlined, because an out-of-line
+// call would put those arrays in local memory for the whole loop.
+template <bool kSum>
+__device__ __forceinline__ float4 move_running_max_regs(const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+                                                        uint32_t (&pk)[32], uint32_t tO, int o_cols, bool need,
+                                                        float m, float sl2, uint32_t pv_bar, uint32_t parity,
+                                                        long long limit, const volatile int* abort_flag) {
+  const float mx = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
+  const float m_new = need ? fmaxf(m, mx) : m;
+  const float corr = m_new == m ? 1.f : ptx::ex2(m - m_new);  // 0 while m is -inf
+  bool ok = true;
+  if (o_cols) {
+    ok = ptx::mbar_wait_warp(pv_bar, parity, limit, abort_flag);
+    ptx::tc_fence_after();
+    rescale_tmem(tO, o_cols, corr);
+  }
+  uint32_t orr;
+  const float sum = exp_pack64<kSum>(sa, sb, sl2, -m_new, pk, &orr);
   return make_float4(m_new, sum, corr, ok ? 1.f : 0.f);
 }
 
@@ -363,13 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int st) { return bars + 8 * st; };
   auto empty_bar = [&](int st) { return bars + 8 * (S + st); };
   const uint32_t q_full = bars + 8 * (2 * S);
+  // head_dim 64 uses s_full / p_ready per (tile, half buffer); head_dim 128 buffer 0 only
   auto s_full = [&](int t, int b) { return q_full + 8 * (1 + 2 * t + b); };
-  auto p_ready = [&](int t, int b) { return q_full + 8 * (5 + 2 * t + b); };
-  auto pv_done = [&](int t) { return q_full + 8 * (9 + t); };
-  auto o_done = [&](int t) { return q_full + 8 * (11 + t); };
-  const uint32_t s2_full = q_full + 8 * 14, s2_free = q_full + 8 * 15;
-  auto p2_ready = [&](int b) { return q_full + 8 * (16 + b); };
-  const uint32_t pv2_done = q_full + 8 * 18;
+  auto s_free = [&](int t) { return q_full + 8 * (5 + t); };
+  auto p_ready = [&](int t, int b) { return q_full + 8 * (7 + 2 * t + b); };
+  auto pv_done = [&](int t) { return q_full + 8 * (11 + t); };
+  auto o_done = [&](int t) { return q_full + 8 * (13 + t); };
+  const uint32_t s2_full = q_full + 8 * 16, s2_free = q_full + 8 * 17;
+  auto p2_ready = [&](int b) { return q_full + 8 * (18 + b); };
+  const uint32_t pv2_done = q_full + 8 * 20;
+  constexpr bool kEarly = C::kEarly;
   const uint32_t sOnes = sbase + C::kOnesBlk;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
@@ -387,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = work.chunk_end - work.chunk_begin;
   const int row0 = group * 2 * kTileRows;
   const int n_main = min(2, p.main_tiles - 2 * group);
-  const bool has_tail = C::kTail && group == p.ngroups - 1 && p.tail_rows > 0;
+  const bool has_tail = group == p.ngroups - 1 && p.tail_rows > 0;
   const int tail_row0 = p.main_tiles * kTileRows;
   const long long limit = p.wait_limit_ns;
   bool dump = false;
@@ -406,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(s_full(t, b), 1);
         ptx::mbar_init(p_ready(t, b), 128);
       }
+      ptx::mbar_init(s_free(t), 128);
       ptx::mbar_init(pv_done(t), 1);
     }
     for (int t = 0; t < 3; ++t) ptx::mbar_init(o_done(t), 1);
@@ -487,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tQ = tmem + (t ? C::kTQ1 : C::kTQ0);
         const uint32_t tO = tmem + (t ? C::kO1 : C::kO0);
         const int halves = dump ? min(2 * n, 2) : 2 * n;
-        // S_t[g % 2] = Q_t K^T over the 64 keys of half chunk g
+        // S = Q_t K^T over the 64 keys of half chunk g, into the buffer of half g
         auto issue_qk = [&](int g) -> bool {
           const int c = g >> 1, st = c % S;
           if ((g & 1) == 0) {
@@ -496,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t == 0) trace<kDiag>(p, kTrFullSeen, c);
           }
           const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep + uint32_t(g & 1) * kHalfRows;
-          const uint32_t tS = tmem + s_col(t, g & 1);
+          const uint32_t tS = tmem + s_col<D>(t, g & 1);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
@@ -508,20 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               else ptx::mma_ss_lh<1>(tS, q_lo + off, k_lo + off, hi, idesc_qk);
             }
           }
-          ptx::mma_commit(s_full(t, g & 1));
-          trace<kDiag>(p, t ? kTrQk1 : ((g & 1) ? kTrQk0h1 : kTrQk0), c);
+          ptx::mma_commit(s_full(t, kEarly ? 0 : (g & 1)));
+          if (t == 0) trace<kDiag>(p, (g & 1) ? kTrQk0h1 : kTrQk0, c);
+          else if ((g & 1) == 0) trace<kDiag>(p, kTrQk1, c);
           return true;
         };
-        for (int g = 0; ok && g < min(halves, 2); ++g) ok = issue_qk(g);
-        for (int g = 0; ok && !dump && g < halves; ++g) {
+        // O_t (+)= P V over the 64 keys of half g: a k-step is 16 key rows (2 KB) of V and 8
+        // TMEM columns of packed P
+        auto issue_pv = [&](int g) {
           const int b = g & 1, c = g >> 1, st = c % S;
-          if (!(ok = ptx::mbar_wait_bounded(p_ready(t, b), c & 1, limit, abort_flag))) break;
-          ptx::tc_fence_after();
-          trace<kDiag>(p, t ? kTrP1Seen : (b ? kTrP0h1Seen : kTrP0Seen), c);
-          // O_t (+)= P V over the half's 64 keys: a k-step is 16 key rows (2 KB) of V and
-          // 8 TMEM columns of packed P
           const uint32_t v_lo = v_lo_of(st) + uint32_t(b) * kHalfRows;
-          const uint32_t tP = tmem + s_col(t, b);
+          const uint32_t tP = tmem + p_col<D>(t, b);
 #pragma unroll
           for (int k = 0; k < kHalfKeys / 16; ++k)
             ptx::mma_ts_lh(tO, tP + 8 * k, v_lo + uint32_t(128 * k), hi, idesc_pv, (g > 0 || k > 0) ? 1u : 0u);
@@ -530,16 +580,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
             if (t == 0) trace<kDiag>(p, kTrEmpty, c);
           }
-          if (g + 2 < halves) ok = issue_qk(g + 2);  // into the buffer the PV above reads (in order)
+        };
+        auto wait_p = [&](int g) -> bool {
+          const int b = g & 1, c = g >> 1;
+          if (!ptx::mbar_wait_bounded(p_ready(t, kEarly ? 0 : b), kEarly ? (g & 1) : (c & 1), limit, abort_flag))
+            return false;
+          ptx::tc_fence_after();
+          if (t == 0) trace<kDiag>(p, b ? kTrP0h1Seen : kTrP0Seen, c);
+          else if (b == 0) trace<kDiag>(p, kTrP1Seen, c);
+          return true;
+        };
+        if constexpr (kEarly) {
+          // one S buffer: Q K^T of half g+1 as soon as the softmax has loaded half g
+          if (halves > 0) ok = ok && issue_qk(0);
+          for (int g = 0; ok && g < halves; ++g) {
+            if (g + 1 < halves) {
+              if (!(ok = ptx::mbar_wait_bounded(s_free(t), g & 1, limit, abort_flag))) break;
+              ptx::tc_fence_after();
+              if (!(ok = issue_qk(g + 1))) break;
+            }
+            if (dump) continue;
+            if (!(ok = wait_p(g))) break;
+            issue_pv(g);
+          }
+        } else {
+          // two S buffers: Q K^T of half g+2 into the buffer the PV of half g reads (in order)
+          for (int g = 0; ok && g < min(halves, 2); ++g) ok = issue_qk(g);
+          for (int g = 0; ok && !dump && g < halves; ++g) {
+            if (!(ok = wait_p(g))) break;
+            issue_pv(g);
+            if (g + 2 < halves) ok = issue_qk(g + 2);
+          }
         }
       } else {
-        // Tail: S2^T = K Q2^T (M = 128 keys, N = 16, K = 64) into one TMEM buffer, then
-        // O2^T (+)= V^T P2^T (M = 64 columns of V, N = 8 tail rows, K = 128 keys): A = V^T
-        // read MN-major from the V tile, B = P2^T K-major from shared memory.  With
-        // M = 64 the accumulator's rows (V columns) 16q..16q+15 live in TMEM lanes
-        // 32q..32q+15.
+        // Tail: S2^T = K Q2^T (M = 128 keys, N = 16, K = D) into one TMEM buffer, then
+        // O2^T (+)= V^T P2^T (M = D columns of V, N = kTailPvN rows, K = 128 keys): A = V^T
+        // read MN-major from the V tile, B = P2^T K-major from shared memory.  With M = 64
+        // the accumulator's rows (V columns) 16q..16q+15 live in TMEM lanes 32q..32q+15;
+        // with M = 128 row i lives in lane i.
         constexpr uint32_t idesc_st = ptx::idesc_bf16_f32(128, kTailN, 0, 0);
-        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(64, kTailMaxRows, 1, 0);
+        constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(D, C::kTailPvN, 1, 0);
         const uint32_t q2_lo = uint32_t(ptx::smem_desc_sw128(sQ2, 16, 1024));
         const uint32_t p2_lo = uint32_t(ptx::smem_desc_sw128(sP2, 16, 1024));
         const uint32_t tS2 = tmem + C::kS2, tO2 = tmem + C::kO2;
@@ -550,9 +630,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t aoff = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
+            const uint32_t boff = uint32_t((k >> 2) * (C::kQ2ColBlock >> 4) + (k & 3) * 2);
             if (k == 0) ptx::mma_ss_lh<0>(tS2, k_lo, q2_lo, hi, idesc_st);
-            else ptx::mma_ss_lh<1>(tS2, k_lo + 2 * k, q2_lo + 2 * k, hi, idesc_st);
+            else ptx::mma_ss_lh<1>(tS2, k_lo + aoff, q2_lo + boff, hi, idesc_st);
           }
           ptx::mma_commit(s2_full);
           trace<kDiag>(p, kTrQk2, c);
@@ -571,10 +653,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           trace<kDiag>(p, kTrP2Seen, c);
           const uint32_t v_lo = v_lo_of(st);
-          const uint32_t b_lo = p2_lo + uint32_t((c & 1) * (kP2Bytes >> 4));
+          const uint32_t b_lo = p2_lo + uint32_t((c & 1) * (C::kP2Bytes >> 4));
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t boff = uint32_t((k >> 2) * (1024 >> 4) + (k & 3) * 2);
+            const uint32_t boff = uint32_t((k >> 2) * (C::kP2ColBlock >> 4) + (k & 3) * 2);
             if (c == 0 && k == 0) ptx::mma_ss_lh<0>(tO2, v_lo, b_lo, hi, idesc_pv);
             else ptx::mma_ss_lh<1>(tO2, v_lo + uint32_t(128 * k), b_lo + boff, hi, idesc_pv);
           }
@@ -597,7 +679,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = tile_on && row < p.T;
     const bool warp_on = tile_on && row0 + t * kTileRows + q4 * 32 < p.T;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    const uint32_t tS0 = tmem + s_col(t, 0) + lane_off;  // buffer b at + 64 b
     const uint32_t tO = tmem + (t ? C::kO1 : C::kO0) + lane_off;
     const int64_t qrow = int64_t(work.stream) * p.T + row;
     const uint4* qsrc =
@@ -634,72 +715,94 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tile_on && dump) {
       if constexpr (kDiag) {
+        // the first chunk's two halves of scores, as the tensor core wrote them
         float* dst = p.dump_scores + ((int64_t(blockIdx.x) * 2 + t) * 128 + r) * 128;
-        for (int b = 0; b < 2 && n > 0; ++b) {
-          if (!ptx::mbar_wait_warp(s_full(t, b), 0, limit, abort_flag)) break;
+        for (int b = 0; b < 2 && b < 2 * n; ++b) {
+          if (!ptx::mbar_wait_warp(s_full(t, kEarly ? 0 : b), kEarly ? b : 0, limit, abort_flag)) break;
           ptx::tc_fence_after();
-          for (int j = 0; j < 2; ++j) {
-            uint32_t s[32];
-            ptx::tmem_ld32(tS0 + kHalfKeys * b + 32 * j, s);
-            ptx::tmem_wait_ld();
-            for (int e = 0; e < 32; ++e) dst[kHalfKeys * b + 32 * j + e] = __uint_as_float(s[e]);
+          uint32_t sd[2][32];
+          const uint32_t tS = tmem + s_col<D>(t, b) + lane_off;
+          ptx::tmem_ld32(tS, sd[0]);
+          ptx::tmem_ld32(tS + 32, sd[1]);
+          ptx::tmem_wait_ld();
+          if constexpr (kEarly) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(s_free(t));
           }
+          for (int j = 0; j < 2; ++j)
+            for (int e = 0; e < 32; ++e) dst[kHalfKeys * b + 32 * j + e] = __uint_as_float(sd[j][e]);
         }
       }
     } else if (tile_on) {
-      float m = -INFINITY;  // running max of scaled logits (log2 units)
+      float m = -INFINITY;  // running max of scaled logits (log2 units); the first half sets it
       float l = 0.f;        // D = 128: running sum of the bf16-rounded P (D = 64 takes it from O)
       bool ok = true;
       int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
-      if (warp_on && n > 0) {
-        // the first half sets the running max from its own scores (nothing to rescale yet)
-        if ((ok = ptx::mbar_wait_warp(s_full(t, 0), 0, limit, abort_flag))) {
-          ptx::tc_fence_after();
-          uint32_t sa[32], sb[32];
-          ptx::tmem_ld32(tS0, sa);
-          ptx::tmem_ld32(tS0 + 32, sb);
-          ptx::tmem_wait_ld();
-          mask32(sa, 0, len_next);
-          mask32(sb, 32, len_next);
-          m = fmaxf(max32(sa, -INFINITY), max32(sb, -INFINITY)) * sl2;
-        }
-      }
       for (int g = 0; ok && g < 2 * n; ++g) {
         const int b = g & 1;
         if (b == 0) {
           len = len_next;
           if ((g >> 1) + 1 < n) len_next = __ldg(&p.chunks[c0 + (g >> 1) + 1].start_len) >> 16;
         }
-        if (!(ok = ptx::mbar_wait_warp(s_full(t, b), (g >> 1) & 1, limit, abort_flag))) break;
+        if (!(ok = ptx::mbar_wait_warp(s_full(t, kEarly ? 0 : b), kEarly ? (g & 1) : ((g >> 1) & 1), limit,
+                                       abort_flag)))
+          break;
         ptx::tc_fence_after();
         if (q4 == 0 && lane == 0) trace<kDiag>(p, t ? kTrS1Seen : (b ? kTrS0h1Seen : kTrS0Seen), g >> 1);
+        const uint32_t tS = tmem + s_col<D>(t, b) + lane_off;
+        uint32_t sa[32], sb[32], pk[32];
+        ptx::tmem_ld32(tS, sa);
+        ptx::tmem_ld32(tS + 32, sb);
+        ptx::tmem_wait_ld();
+        if constexpr (kEarly) {  // the scores are in registers: the buffer goes back to the issuer
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(s_free(t));
+        }
+        bool waited_pv = g == 0;  // the previous half's PV (none before half 0)
+        bool p_stored = false;
         if (warp_on) {
-          // The half's 64 scores are exponentiated against the running max m; only when
-          // some P value reaches 2 (a rare jump of the max) does the warp take the
-          // out-of-line path that moves m, rescales O and recomputes this half's P.
-          // P (packed bf16 pairs) overwrites the first 32 columns of the half's S buffer.
-          const uint32_t tS = tS0 + kHalfKeys * b;
-          uint32_t sa[32], sb[32], pk[32], orr;
-          ptx::tmem_ld32(tS, sa);
-          ptx::tmem_ld32(tS + 32, sb);
-          ptx::tmem_wait_ld();
+          // exponentiated against the running max m; only when some P value reaches 2 (the
+          // first half, and rare jumps of the max) does the warp take the path that moves
+          // m, rescales O and recomputes this half's P
           mask32(sa, kHalfKeys * b, len);
           mask32(sb, kHalfKeys * b + 32, len);
+          uint32_t orr;
           const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk, &orr);
           const bool need = (orr & kPHighBits) != 0;
           if (__any_sync(0xffffffffu, need)) {
-            const float4 r4 = move_running_max<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, need, m, sl2, kHalfKeys * b,
-                                                           len, pv_done(t), uint32_t(g - 1) & 1u, limit, abort_flag);
+            float4 r4;
+            if constexpr (kEarly) {
+              r4 = move_running_max_regs<!C::kOnes>(sa, sb, pk, tO, g > 0 ? C::kOW : 0, need, m, sl2, pv_done(t),
+                                                    uint32_t(g - 1) & 1u, limit, abort_flag);
+            } else {
+              r4 = move_running_max_tmem<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, need, m, sl2, kHalfKeys * b, len,
+                                                    pv_done(t), uint32_t(g - 1) & 1u, limit, abort_flag);
+              p_stored = true;
+            }
             if constexpr (!C::kOnes) l = l * r4.z + r4.y;
             m = r4.x;
+            waited_pv = true;
+            if constexpr (kDiag)  // diagnostics: count rescales of an accumulated O (any CTA)
+              if (p.trace != nullptr && g > 0 && lane == 0) atomicAdd(p.trace + int64_t(kTraceEvents) * p.trace_cap, 1ull);
             if (r4.w == 0.f) {
               ok = false;
               break;
             }
           } else {
-            ptx::tmem_st32(tS, pk);
             if constexpr (!C::kOnes) l += ps;
+          }
+          if (!kEarly && !p_stored) {  // P over the scores it came from
+            ptx::tmem_st32(tS, pk);
+            ptx::tmem_wait_st();
+          }
+        }
+        if constexpr (kEarly) {
+          // the tile's P buffer: the previous half's PV must have read it
+          if (!waited_pv && !(ok = ptx::mbar_wait_warp(pv_done(t), uint32_t(g - 1) & 1u, limit, abort_flag))) break;
+          ptx::tc_fence_after();
+          if (warp_on) {
+            ptx::tmem_st32(tmem + p_col<D>(t, b) + lane_off, pk);
             ptx::tmem_wait_st();
           }
         }
@@ -712,8 +815,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // an arrive releases this thread's earlier writes, so the trace store follows it
         long long t_arrive = 0;
         if constexpr (kDiag) t_arrive = clock64();
-        ptx::mbar_arrive(p_ready(t, b));
-        if (q4 == 0 && lane == 0)
+        ptx::mbar_arrive(p_ready(t, kEarly ? 0 : b));
+        if (q4 == 0 && lane == 0 && (t == 0 || b == 0))
           trace_at<kDiag>(p, t ? kTrP1Arrive : (b ? kTrP0h1Arrive : kTrP0Arrive), g >> 1, t_arrive);
       }
       if (!ok) signal_abort(p.status, abort_flag);
@@ -736,9 +839,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_ok && work.nsplit > 1) p.part_lse[(int64_t(split) * p.H + head) * p.T + row] = m + __log2f(l);
       }
     }
-  } else if constexpr (!C::kTail) {
-    // warps 0-3 have no tail to work on; they still count towards q_full
-    ptx::mbar_arrive(q_full);
   } else {
     // ------------------------------------------------------------ tail softmax (warps 0-3)
     const int q = warp;  // key group [32q, 32q+32) of each chunk; TMEM lane quarter q
@@ -752,19 +852,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* xok = reinterpret_cast<int*>(xmax + 2 * 4 * kTailMaxRows);
     if (has_tail) {
       // zero both P tiles (rows past tail_rows stay zero), then stage the tail's Q rows
-      // (rows past tail_rows are zero) as the B operand of S2^T
-      for (int i = tid; i < 2 * kP2Bytes / 16; i += 128) st_shared_zero16(sP2 + uint32_t(i * 16));
-      const int qr = tid >> 3, qc = tid & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (qr < tail_rows) {
-        const int64_t qrow = int64_t(work.stream) * p.T + tail_row0 + qr;
-        v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D) +
-                  qc);
+      // (rows past tail_rows are zero) as the B operand of S2^T: 16 rows, D/64 column blocks
+      for (int i = tid; i < 2 * C::kP2Bytes / 16; i += 128) st_shared_zero16(sP2 + uint32_t(i * 16));
+      for (int u = tid; u < kTailN * (D / 8); u += 128) {
+        const int qr = u / (D / 8), qc = u % (D / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (qr < tail_rows) {
+          const int64_t qrow = int64_t(work.stream) * p.T + tail_row0 + qr;
+          v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) + (qrow * p.H + head) * D) +
+                    qc);
+        }
+        const uint32_t dst = sQ2 + uint32_t((qc >> 3) * C::kQ2ColBlock + (qr >> 3) * 1024 + (qr & 7) * 128 +
+                                            (((qc & 7) ^ (qr & 7)) << 4));
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
       }
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sQ2 + uint32_t((qr >> 3) * 1024 + (qr & 7) * 128 +
-                                                                                 ((qc ^ (qr & 7)) << 4))),
-                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
     }
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(q_full);
@@ -845,15 +947,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rr = 0; rr < kTailMaxRows; ++rr) o[rr] = __float_as_uint(__uint_as_float(o[rr]) * corr[rr]);
             ptx::tmem_st8(tO2, o);
             ptx::tmem_wait_st();
+            if constexpr (kDiag)
+              if (p.trace != nullptr && lane == 0) atomicAdd(p.trace + int64_t(kTraceEvents) * p.trace_cap + 1, 1ull);
           }
         }
-        const uint32_t p2 = sP2 + uint32_t((j & 1) * kP2Bytes);
+        const uint32_t p2 = sP2 + uint32_t((j & 1) * C::kP2Bytes);
 #pragma unroll
         for (int rr = 0; rr < kTailMaxRows; ++rr) {
           if (rr < tail_rows) {
             const __nv_bfloat16 pb = __float2bfloat16_rn(ptx::ex2(xs[rr] - m[rr]));
             l[rr] += __bfloat162float(pb);
-            st_shared_u16(p2_addr(p2, rr, key), __bfloat16_as_ushort(pb));
+            st_shared_u16(p2_addr(p2, C::kP2ColBlock, rr, key), __bfloat16_as_ushort(pb));
           }
         }
         if (len < kChunkTokens) zero_v_rows<D>(sV(j % S), len, kChunkTokens, tid, 128);
@@ -883,10 +987,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (done && !*abort_flag) {
         ptx::tc_fence_after();
         uint32_t o[8];
-        ptx::tmem_ld8(tO2, o);  // lane i < 16 of quarter q: column 16q + i of V, the 8 rows
+        ptx::tmem_ld8(tO2, o);  // this lane's column of V (see below), the first 8 rows
         ptx::tmem_wait_ld();
-        if (lane < 16) {
-          const int d = 16 * q + lane;
+        // M = 64: lanes 0-15 of quarter q hold V columns 16q..16q+15; M = 128: lane i of
+        // quarter q holds column 32q + i
+        constexpr int kLanesUsed = D == 64 ? 16 : 32;
+        if (lane < kLanesUsed) {
+          const int d = kLanesUsed * q + lane;
 #pragma unroll
           for (int rr = 0; rr < kTailMaxRows; ++rr) {
             if (rr < tail_rows) {
@@ -951,7 +1058,7 @@ cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map
 TileShape attention_bf16_tiles(int T, int head_dim) {
   TileShape ts{};
   const int full = T / kTileRows, rem = T % kTileRows;
-  if (head_dim == 64 && rem > 0 && rem <= kTailMaxRows) {
+  if (rem > 0 && rem <= kTailMaxRows) {
     ts.main_tiles = full;
     ts.tail_rows = rem;
   } else {

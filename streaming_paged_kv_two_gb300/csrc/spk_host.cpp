@@ -283,8 +283,8 @@ int choose_splits(const spk_cache* c, const std::vector<int32_t>& nchunks, std::
     per_split_ctas = B * g.num_heads * attention_bf16_tiles(c->Tq, g.head_dim).ngroups;
     slots = c->num_sms;
   } else {
-    per_split_ctas = B * g.num_heads * ((c->Tq + 7) / 8);
-    slots = c->num_sms * 8;
+    per_split_ctas = B * g.num_heads * f32_row_tiles(c->Tq);
+    slots = c->num_sms * 2;
   }
   const double overhead_chunks = 2.0, split_charge = 0.25;
   int best = 1;
@@ -363,7 +363,7 @@ int build_plan(spk_cache* c) {
   c->info.num_chunks = int32_t(c->chunks.size());
   c->info.num_splits = int32_t(c->works.size());
   c->info.num_ctas = int32_t(c->works.size()) * g.num_heads *
-                     (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->Tq, g.head_dim).ngroups : (c->Tq + 7) / 8);
+                     (g.dtype == SPK_BF16 ? attention_bf16_tiles(c->Tq, g.head_dim).ngroups : f32_row_tiles(c->Tq));
   c->info.merge_needed = merge ? 1 : 0;
   c->info.visible_tokens = visible;
   c->info.split_scratch_bytes = merge ? int64_t(split_scratch_bytes(c)) : 0;
@@ -463,6 +463,10 @@ int spk_create_cache(const spk_config* cfg, void* const* pools, spk_cache** out)
     // current: spk_run_attention_static_scratch then reserves nothing when it runs.
     e = static_scratch_address(&c->static_scratch);
     if (e != cudaSuccess) return bail(cuda_fail(e, "static scratch address"));
+    if (cfg->dtype == SPK_F32) {
+      e = configure_attention_f32();
+      if (e != cudaSuccess) return bail(cuda_fail(e, "fp32 attention kernel configuration"));
+    }
     if (cfg->dtype == SPK_BF16) {
       e = configure_attention_bf16();
       if (e != cudaSuccess) return bail(cuda_fail(e, "attention kernel configuration"));

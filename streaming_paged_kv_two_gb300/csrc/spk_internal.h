@@ -145,6 +145,10 @@ cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map
 // bf16 attention kernels.
 cudaError_t configure_attention_bf16();
 cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s);
+// Once per fp32 cache, with its device current: dynamic shared memory of the fp32 kernels.
+cudaError_t configure_attention_f32();
+// CTAs of the fp32 attention kernel per (split, head) for T query rows.
+int f32_row_tiles(int T);
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, long long limit_ns, cudaStream_t s);
 

@@ -132,80 +132,248 @@ cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ fp32 attention
-// Accuracy path (SPK_F32): exact attention over the split's chunks in fp32 on
-// CUDA cores, the paged counterpart of the manager's force_fp32 dense path ("How
-// LingBot-Map Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "Attention
-// Kernel Execution").  One warp per (query row, head); lanes split D; online
-// softmax in log2 units.
+// Accuracy path (SPK_F32): exact attention over the split's chunks in fp32 on the CUDA
+// cores, the paged counterpart of the manager's force_fp32 dense path ("How LingBot-Map
+// Uses FlashInfer KV Cache for Streaming 3D Reconstruction", "Attention Kernel
+// Execution"; "How FlashInfer's Paged KV Cache Attention Outperforms SDPA Fallback in
+// Streaming Inference", "Precision and Hardware Utilization").
+// One CTA = (KV split, head, 64 query rows), 256 threads as 16 x 16: thread (ty, tx)
+// owns rows 4ty..4ty+3; for S it computes keys tx + 16j (j < 4) of each 64-key tile,
+// for O the columns [tx*D/16, (tx+1)*D/16).  Q (scaled to log2 units) stays in shared
+// memory; K and V arrive in 64-key tiles (each a piece of one planner chunk, rows past
+// its length zero-filled) through a double-buffered cp.async ring, so every visible key
+// is read from memory once per CTA.  Online softmax in log2 units: per tile, the row max
+// over the 16 threads of a row (shuffles), O rescaled when it grows, P written
+// transposed to shared memory for the P V product.
+constexpr int kF32Rows = 64;
+constexpr int kF32Keys = 64;
+constexpr int kF32Threads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(256) attention_f32_kernel(const AttnParams p) {
-  constexpr int E = D / 32;
-  constexpr int kRowsPerCta = 8;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int row_tiles = (p.T + kRowsPerCta - 1) / kRowsPerCta;
-  int x = blockIdx.x;
-  const int rt = x % row_tiles;
-  x /= row_tiles;
-  const int h = x % p.H;
-  const int split = x / p.H;
-  const int t = rt * kRowsPerCta + warp;
-  if (t >= p.T) return;
-  const WorkDesc w = p.works[split];
-  const float* pool = static_cast<const float*>(p.pool);
-  const int64_t qrow = int64_t(w.stream) * p.T + t;
-  const float* qp = static_cast<const float*>(p.q) + (qrow * p.H + h) * D + lane * E;
-  float q[E], acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    q[e] = qp[e] * p.scale_log2;
-    acc[e] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
-  for (int c = w.chunk_begin; c < w.chunk_end; ++c) {
+struct F32Cfg {
+  static constexpr int kLd = D + 4;  // shared row stride in floats (16-byte aligned, no bank conflicts)
+  static constexpr int kTileFloats = kF32Keys * kLd;
+  static constexpr int kQ = 0;
+  static constexpr int kKV = kF32Rows * kLd;              // [2 buffers][K, V][64][kLd]
+  static constexpr int kP = kKV + 4 * kTileFloats;        // P^T [64 keys][68]
+  static constexpr int kFloats = kP + kF32Keys * (kF32Rows + 4);
+  static constexpr int kBytes = kFloats * 4;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// The k-th 64-key tile of the split: walks the chunk list (a chunk of len keys gives
+// ceil(len / 64) tiles).  Returns false past the split's end.
+struct F32Tile {
+  int page, start, len;  // pool page, first token, valid keys (<= 64)
+};
+__device__ __forceinline__ bool next_f32_tile(const AttnParams& p, int& c, int& h, int c_end, F32Tile& t) {
+  while (c < c_end) {
     const ChunkDesc cd = p.chunks[c];
-    const int start = cd.start_len & 0xFFFF;
     const int len = cd.start_len >> 16;
-    const float* kbase = pool + int64_t(cd.page) * p.page_stride + int64_t(start) * p.row_stride + h * D + lane * E;
-    const float* vbase = kbase + p.half_stride;
-    for (int j = 0; j < len; ++j) {
-      const float* kr = kbase + int64_t(j) * p.row_stride;
-      float s = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) s = fmaf(q[e], __ldg(kr + e), s);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      const float m_new = fmaxf(m, s);
-      const float corr = exp2f(m - m_new);
-      const float pj = exp2f(s - m_new);
-      const float* vr = vbase + int64_t(j) * p.row_stride;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], corr, pj * __ldg(vr + e));
-      l = fmaf(l, corr, pj);
-      m = m_new;
+    if (h * kF32Keys < len) {
+      t.page = cd.page;
+      t.start = (cd.start_len & 0xFFFF) + h * kF32Keys;
+      t.len = min(kF32Keys, len - h * kF32Keys);
+      ++h;
+      return true;
     }
+    ++c;
+    h = 0;
   }
-  const float inv = 1.f / l;
-  if (w.nsplit == 1) {
-    float* o = static_cast<float*>(p.out) + (qrow * p.H + h) * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = acc[e] * inv;
-  } else {
-    const int64_t idx = (int64_t(split) * p.H + h) * p.T + t;
-#pragma unroll
-    for (int e = 0; e < E; ++e) p.part_o[part_o_offset<D>(split, h, t, lane * E + e, p.H, p.T)] = acc[e] * inv;
-    if (lane == 0) p.part_lse[idx] = m + log2f(l);
+  return false;
+}
+
+template <int D>
+__device__ __forceinline__ void load_f32_tile(const AttnParams& p, int head, const F32Tile& t, uint32_t sk, uint32_t sv) {
+  using C = F32Cfg<D>;
+  const float* pool = static_cast<const float*>(p.pool);
+  const float* kbase = pool + int64_t(t.page) * p.page_stride + int64_t(t.start) * p.row_stride + int64_t(head) * D;
+  constexpr int kVec = D / 4;  // float4 per key row
+  for (int i = threadIdx.x; i < kF32Keys * kVec; i += kF32Threads) {
+    const int key = i / kVec, c4 = i % kVec;
+    const bool valid = key < t.len;
+    const float* src = kbase + int64_t(valid ? key : 0) * p.row_stride + 4 * c4;
+    const uint32_t off = uint32_t((key * C::kLd + 4 * c4) * 4);
+    cp_async16(sk + off, src, valid);
+    cp_async16(sv + off, src + p.half_stride, valid);
   }
 }
 
+template <int D>
+__global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(const AttnParams p) {
+  using C = F32Cfg<D>;
+  constexpr int kCols = D / 16;  // O columns per thread
+  extern __shared__ float4 f32_smem4[];
+  float* sm = reinterpret_cast<float*>(f32_smem4);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int row_tiles = (p.T + kF32Rows - 1) / kF32Rows;
+  int x = blockIdx.x;
+  const int rt = x % row_tiles;
+  x /= row_tiles;
+  const int head = x % p.H;
+  const int split = x / p.H;
+  const WorkDesc w = p.works[split];
+
+  // Q tile (rows past T are zero), scaled to log2 units
+  float* Qs = sm + C::kQ;
+  for (int i = tid; i < kF32Rows * (D / 4); i += kF32Threads) {
+    const int r = i / (D / 4), c4 = i % (D / 4);
+    const int t = rt * kF32Rows + r;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < p.T) {
+      v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.q) +
+                                                ((int64_t(w.stream) * p.T + t) * p.H + head) * D) + c4);
+      v.x *= p.scale_log2;
+      v.y *= p.scale_log2;
+      v.z *= p.scale_log2;
+      v.w *= p.scale_log2;
+    }
+    *reinterpret_cast<float4*>(Qs + r * C::kLd + 4 * c4) = v;
+  }
+  float* Ps = sm + C::kP;  // P^T: [key][row], row stride 68
+  auto sk = [&](int b) { return sbase + uint32_t((C::kKV + (2 * b) * C::kTileFloats) * 4); };
+  auto sv = [&](int b) { return sbase + uint32_t((C::kKV + (2 * b + 1) * C::kTileFloats) * 4); };
+  const float* Ks_base = sm + C::kKV;
+
+  float m[4], l[4], o[4][kCols];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) o[r][c] = 0.f;
+  }
+  int c = w.chunk_begin, h = 0;
+  F32Tile cur, nxt;
+  bool have = next_f32_tile(p, c, h, w.chunk_end, cur);
+  if (have) load_f32_tile<D>(p, head, cur, sk(0), sv(0));
+  cp_async_commit();
+  for (int it = 0; have; ++it) {
+    const int b = it & 1;
+    const bool more = next_f32_tile(p, c, h, w.chunk_end, nxt);
+    if (more) load_f32_tile<D>(p, head, nxt, sk(b ^ 1), sv(b ^ 1));
+    cp_async_commit();
+    cp_async_wait<1>();  // this tile's copies have landed
+    __syncthreads();
+    const float* Ks = Ks_base + (2 * b) * C::kTileFloats;
+    const float* Vs = Ks_base + (2 * b + 1) * C::kTileFloats;
+    // S = Q K^T for rows 4ty.. and keys tx + 16j
+    float s[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[r][j] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; d += 4) {
+      float4 q4[4], k4[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) q4[r] = *reinterpret_cast<const float4*>(Qs + (4 * ty + r) * C::kLd + d);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) k4[j] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * j) * C::kLd + d);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          s[r][j] = fmaf(q4[r].x, k4[j].x, fmaf(q4[r].y, k4[j].y, fmaf(q4[r].z, k4[j].z, fmaf(q4[r].w, k4[j].w, s[r][j]))));
+    }
+    // online softmax over the tile's valid keys
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (tx + 16 * j >= cur.len) s[r][j] = -INFINITY;
+        mx = fmaxf(mx, s[r][j]);
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m[r], mx);  // finite: every tile has at least one valid key
+      const float corr = exp2f(m[r] - m_new);
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float pj = exp2f(s[r][j] - m_new);
+        Ps[(tx + 16 * j) * (kF32Rows + 4) + 4 * ty + r] = pj;
+        sum += pj;
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      l[r] = l[r] * corr + sum;
+      m[r] = m_new;
+#pragma unroll
+      for (int cc = 0; cc < kCols; ++cc) o[r][cc] *= corr;
+    }
+    __syncthreads();
+    // O += P V over the tile's keys (keys past len have P = 0 and zero-filled V rows)
+#pragma unroll 4
+    for (int j = 0; j < kF32Keys; ++j) {
+      const float4 p4 = *reinterpret_cast<const float4*>(Ps + j * (kF32Rows + 4) + 4 * ty);
+      const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+      for (int q = 0; q < kCols / 4; ++q) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * C::kLd + tx * kCols + 4 * q);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          o[r][4 * q] = fmaf(pr[r], v4.x, o[r][4 * q]);
+          o[r][4 * q + 1] = fmaf(pr[r], v4.y, o[r][4 * q + 1]);
+          o[r][4 * q + 2] = fmaf(pr[r], v4.z, o[r][4 * q + 2]);
+          o[r][4 * q + 3] = fmaf(pr[r], v4.w, o[r][4 * q + 3]);
+        }
+      }
+    }
+    __syncthreads();  // the buffers and P^T are rewritten next
+    cur = nxt;
+    have = more;
+  }
+  cp_async_wait<0>();
+  // epilogue: rows of this tile that exist
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int t = rt * kF32Rows + 4 * ty + r;
+    if (t >= p.T) continue;
+    const float inv = 1.f / l[r];
+    if (w.nsplit == 1) {
+      float* out = static_cast<float*>(p.out) + ((int64_t(w.stream) * p.T + t) * p.H + head) * D + tx * kCols;
+#pragma unroll
+      for (int q = 0; q < kCols / 4; ++q)
+        *reinterpret_cast<float4*>(out + 4 * q) =
+            make_float4(o[r][4 * q] * inv, o[r][4 * q + 1] * inv, o[r][4 * q + 2] * inv, o[r][4 * q + 3] * inv);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kCols / 4; ++q)
+        *reinterpret_cast<float4*>(p.part_o + part_o_offset<D>(split, head, t, tx * kCols + 4 * q, p.H, p.T)) =
+            make_float4(o[r][4 * q] * inv, o[r][4 * q + 1] * inv, o[r][4 * q + 2] * inv, o[r][4 * q + 3] * inv);
+      if (tx == 0) p.part_lse[(int64_t(split) * p.H + head) * p.T + t] = m[r] + log2f(l[r]);
+    }
+  }
+}
+
+cudaError_t configure_attention_f32() {
+  cudaError_t e = cudaFuncSetAttribute(attention_f32_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       F32Cfg<64>::kBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attention_f32_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              F32Cfg<128>::kBytes);
+}
+
 cudaError_t launch_attention_f32(const AttnParams& p, cudaStream_t s) {
-  const int row_tiles = (p.T + 7) / 8;
+  const int row_tiles = (p.T + kF32Rows - 1) / kF32Rows;
   const int64_t blocks = int64_t(p.num_splits) * p.H * row_tiles;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  if (p.D == 64) attention_f32_kernel<64><<<int(blocks), 256, 0, s>>>(p);
-  else attention_f32_kernel<128><<<int(blocks), 256, 0, s>>>(p);
+  if (blocks <= 0 || blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (p.D == 64) attention_f32_kernel<64><<<int(blocks), kF32Threads, F32Cfg<64>::kBytes, s>>>(p);
+  else attention_f32_kernel<128><<<int(blocks), kF32Threads, F32Cfg<128>::kBytes, s>>>(p);
   return cudaGetLastError();
 }
+
+int f32_row_tiles(int T) { return (T + kF32Rows - 1) / kF32Rows; }
 
 // ------------------------------------------------------------------ wait self-test
 // Waits on an mbarrier that nothing signals; the bounded wait gives up after
