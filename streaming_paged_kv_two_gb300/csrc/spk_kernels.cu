@@ -51,48 +51,63 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
 // M = max_j lse_j (log2 units) and w_j = 2^(lse_j - M),
 // out = sum_j w_j O_j / sum_j w_j.  One thread per (stream, head, 4 columns, query
 // row), rows fastest, so a warp reads 32 consecutive rows' float4s of a split in one
-// 512-byte run; the split loop is unrolled so the loads of several splits are in flight.
+// 512-byte run.  The kernel is a chain of memory latencies, not a bandwidth problem
+// (a few MB for the whole grid), so every split's log-sum-exp and partial of a group of
+// kMergeGroup splits is requested at once (predicated loads, no branch between them) and
+// the groups are combined online: M is raised group by group and the sums rescaled.
+constexpr int kMergeGroup = 16;
+
 template <int D, typename OutT>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   // launched as a programmatic dependent of the attention kernel: wait until that grid
   // has completed and its partials are visible (returns at once otherwise)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int V = D / 4;  // float4 per row
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = int64_t(p.B) * p.H * V * p.T;
-  if (idx >= total) return;
-  const int t = int(idx % p.T);
-  int64_t rest = idx / p.T;
-  const int c4 = int(rest % V);
-  rest /= V;
-  const int h = int(rest % p.H);
-  const int s = int(rest / p.H);
+  const int per_head = V * p.T;
+  const int idx = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);  // < B * H * V * T < 2^31 (host check)
+  if (idx >= p.B * p.H * per_head) return;
+  const int sh = idx / per_head;  // stream * H + head
+  const int rem = idx - sh * per_head;
+  const int c4 = rem / p.T;
+  const int t = rem - c4 * p.T;
+  const int s = sh / p.H, h = sh - s * p.H;
   const StreamDesc sd = p.streams[s];
-  if (sd.nsplit <= 1) return;  // written by the attention kernel
-  const int64_t lse0 = (int64_t(sd.split_base) * p.H + h) * p.T + t;  // split 0's log-sum-exp
-  const int64_t lse_step = int64_t(p.H) * p.T;                         // next split, same (head, row)
-  const int64_t o0 = part_o_offset<D>(sd.split_base, h, t, 4 * c4, p.H, p.T);
+  const int n = sd.nsplit;
+  if (n <= 1) return;  // written by the attention kernel
+  const float* lse_p = p.part_lse + (int64_t(sd.split_base) * p.H + h) * p.T + t;  // split 0's log-sum-exp
+  const int64_t lse_step = int64_t(p.H) * p.T;                                     // next split, same (head, row)
+  const float* o_p = p.part_o + part_o_offset<D>(sd.split_base, h, t, 4 * c4, p.H, p.T);
   const int64_t o_step = int64_t(p.H) * D * p.T;
-  // every split's log-sum-exp in flight at once, then the weights
-  float lse[kMaxSplitsPerStream];
-#pragma unroll
-  for (int j = 0; j < kMaxSplitsPerStream; ++j)
-    lse[j] = j < sd.nsplit ? __ldg(&p.part_lse[lse0 + j * lse_step]) : -INFINITY;
-  float m = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < kMaxSplitsPerStream; ++j) m = fmaxf(m, lse[j]);
+  float m = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
+  for (int j0 = 0; j0 < n; j0 += kMergeGroup) {
+    float l[kMergeGroup];
+    float4 v[kMergeGroup];
 #pragma unroll
-  for (int j = 0; j < kMaxSplitsPerStream; ++j) {
-    if (j < sd.nsplit) {
-      const float w = exp2f(lse[j] - m);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + o0 + j * o_step));
+    for (int g = 0; g < kMergeGroup; ++g) {
+      const bool in = j0 + g < n;
+      l[g] = in ? __ldg(lse_p + (j0 + g) * lse_step) : -INFINITY;
+      v[g] = in ? __ldg(reinterpret_cast<const float4*>(o_p + (j0 + g) * o_step)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float gm = m;
+#pragma unroll
+    for (int g = 0; g < kMergeGroup; ++g) gm = fmaxf(gm, l[g]);
+    // the first group's own split 0 is present, so gm is finite from the first group on
+    const float r = gm == m ? 1.f : exp2f(m - gm);
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+    wsum *= r;
+    m = gm;
+#pragma unroll
+    for (int g = 0; g < kMergeGroup; ++g) {
+      const float w = exp2f(l[g] - m);  // 0 for the splits past n
       wsum += w;
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+      acc.x = fmaf(w, v[g].x, acc.x);
+      acc.y = fmaf(w, v[g].y, acc.y);
+      acc.z = fmaf(w, v[g].z, acc.z);
+      acc.w = fmaf(w, v[g].w, acc.w);
     }
   }
   const float inv = 1.f / wsum;
@@ -111,6 +126,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 
 cudaError_t launch_merge(const MergeParams& p, int dtype, cudaStream_t s) {
   const int64_t threads = int64_t(p.B) * p.T * p.H * (p.D / 4);
+  if (threads + 255 > INT32_MAX) return cudaErrorInvalidValue;  // the kernel indexes threads in 32 bits
   const int blocks = int((threads + 255) / 256);
   // programmatic dependent launch: the merge grid may be scheduled while the attention
   // kernel still runs (that kernel signals early); its griddepcontrol.wait orders it
