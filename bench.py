@@ -565,7 +565,8 @@ def run_gpu(args, w: wl.Workload):
                                      f"{peak_kind} (bf16_tflops)"),
                      "avg_launch_us": avg_launch * 1e6, "algorithmic_bytes_per_launch": byts,
                      "algorithmic_flops_per_launch": flops,
-                     "tensor_tflops": flops / avg_launch / 1e12, "hbm_gbs": byts / avg_launch / 1e9},
+                     "tensor_tflops": flops / avg_launch / 1e12, "hbm_gbs": byts / avg_launch / 1e9,
+                     **({"frac_of_sustained": achieved / tflops_sus} if bound == "tensor" else {})},
         "attention_roofline_frac": t_roof_block * L / (max_elapsed / K),
         "roofline_frame_steps_per_s": 1.0 / (t_roof_block * L),
         "e2e": {"value": aggregate_throughput(K, world, e2e_elapsed), "unit": UNIT,

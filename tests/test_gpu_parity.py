@@ -240,6 +240,9 @@ CASES = {
     "t144_rem16_main": (small(patches_per_frame=138, page_size=256, frames=6), 2),
     "t150_rem22_main": (small(patches_per_frame=144, page_size=256, frames=6), 0),
     "t6_tail_only": (small(patches_per_frame=3, specials_per_frame=3, page_size=16, frames=10), 2),
+    # more than 16 splits per stream: the merge combines its groups of 16 splits online
+    "t262_d64_split24": (small(sliding_window=12, frames=16), 24),
+    "f32_split20": (small(dtype="f32", sliding_window=12, frames=14, value_scale=1.0), 20),
 }
 
 
