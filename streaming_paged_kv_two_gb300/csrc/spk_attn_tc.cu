@@ -94,9 +94,13 @@ struct Cfg {
   static constexpr int kP2ColBlock = kTailPvN * 128;  // one 64-key column block of a tail P tile
   static constexpr int kP2Bytes = 2 * kP2ColBlock;    // one tail P tile: kTailPvN rows x 128 keys bf16
   static constexpr int kQ2ColBlock = kTailN * 128;    // one 64-dim column block of the tail Q tile
-  // D == 64: the row sums come out of the PV MMA, whose B operand is V extended by a
-  // 16-column block of ones (O gets 16 more columns, each holding the row sum)
-  static constexpr bool kOnes = (D == 64);
+  // the row sums come out of the PV MMA, whose B operand is V extended by a 16-column
+  // block of ones (O gets 16 more columns, each holding the row sum)
+  static constexpr bool kOnes = true;
+  // D == 128: V has two column blocks, so the ones block must be the third at the same
+  // stride (the MMA's leading offset) from each stage's V: each stage puts its second V
+  // block halfway between its first and the one shared ones block (see the layout below)
+  static constexpr bool kSplitV = (D == 128);
   // D == 64: Q lives in TMEM as the A operand of Q K^T
   static constexpr bool kQTmem = (D == 64);
   // D == 128: one S buffer per tile, released once loaded, and a separate P buffer
@@ -109,8 +113,21 @@ struct Cfg {
   static constexpr int kP2 = kQ2 + (D / 64) * kQ2ColBlock;         // two tail P tiles
   static constexpr int kKV = align1024(kP2 + 2 * kP2Bytes);
   static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kOnesBlk = kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones (kOnes)
-  static constexpr int kTailX = kOnesBlk + (kOnes ? kColBlockBytes : 0);  // tail exchange: [2][4][8] maxima, [2][4] flags
+  // D == 128, in 16 KB column blocks: Q0 Q1 (0-3), Q2 and P2 (4), K of stage 1 (5-6), V0 of
+  // stage 1 (7), K of stage 0 (8-9), V1 of stage 1 (10), V0 of stage 0 (11), V1 of stage 0
+  // (12), ones (13): stage 0's V blocks and the ones block are 1 block apart, stage 1's 3
+  static constexpr int kOnesBlk = kSplitV ? 13 * kColBlockBytes : kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones
+  static constexpr int kTailX = kOnesBlk + (kOnes ? kColBlockBytes : 0);
+  // K tile, V column block 0 and V column block 1 of stage st (byte offsets)
+  __host__ __device__ static constexpr int k_off(int st) {
+    return kSplitV ? (st ? 5 : 8) * kColBlockBytes : kKV + st * kStageBytes;
+  }
+  __host__ __device__ static constexpr int v_off(int st) {
+    return kSplitV ? (st ? 7 : 11) * kColBlockBytes : kKV + st * kStageBytes + kTile;
+  }
+  __host__ __device__ static constexpr int v1_off(int st) {
+    return kSplitV ? (st ? 10 : 12) * kColBlockBytes : v_off(st) + kColBlockBytes;
+  }  // tail exchange: [2][4][8] maxima, [2][4] flags
   static constexpr int kBars = kTailX + (kTail ? 2 * 4 * (kTailMaxRows + 1) * 4 + 32 : 0);
   // full[S], empty[S], q_full, s_full[2][2], s_free[2], p_ready[2][2], pv_done[2], o_done[3],
   // s2_full, s2_free, p2_ready[2], pv2_done
@@ -125,6 +142,10 @@ struct Cfg {
   static constexpr uint32_t kTQ0 = kO1 + kOW, kTQ1 = kTQ0 + (kQTmem ? D / 2 : 0);  // D == 64: Q0, Q1
   static constexpr uint32_t kS2 = kTQ1 + (kQTmem ? D / 2 : 0), kO2 = kS2 + kTailN;  // S2^T, O2^T
   static_assert(kO2 + kTailPvN <= 512, "TMEM budget");
+  static_assert(!kSplitV || (kStages == 2 && kP2 + 2 * kP2Bytes <= 5 * kColBlockBytes &&
+                             kOnesBlk - v_off(0) == 2 * (v1_off(0) - v_off(0)) &&
+                             kOnesBlk - v_off(1) == 2 * (v1_off(1) - v_off(1))),
+                "split V layout: the ones block is the third block at each stage's V stride");
   static_assert(kKV % 1024 == 0 && kP2 % 1024 == 0 && kQ2 % 1024 == 0 && kOnesBlk % 1024 == 0 &&
                 kP2ColBlock % 1024 == 0 && kQ2ColBlock % 1024 == 0,
                 "128-byte-swizzled tiles start on 1024-byte boundaries");
@@ -191,15 +212,15 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
-// Zero key rows [r0, r1) of a 128-key V tile (D/64 column blocks of 128-byte rows; the
-// swizzle only permutes 16-byte pieces inside a row, so a whole row is zeroed as it
-// lies) with `nthreads` threads, this one being `tid`.
+// Zero key rows [r0, r1) of a 128-key V tile (D/64 column blocks of 128-byte rows, the
+// first at sv0, the second at sv1; the swizzle only permutes 16-byte pieces inside a row,
+// so a whole row is zeroed as it lies) with `nthreads` threads, this one being `tid`.
 template <int D>
-__device__ __forceinline__ void zero_v_rows(uint32_t sv, int r0, int r1, int tid, int nthreads) {
+__device__ __forceinline__ void zero_v_rows(uint32_t sv0, uint32_t sv1, int r0, int r1, int tid, int nthreads) {
   const int units = (r1 - r0) * 8;  // 16-byte pieces per column block
   for (int i = tid; i < units * (D / 64); i += nthreads) {
     const int cb = i / units, u = i - cb * units;
-    st_shared_zero16(sv + uint32_t(cb * kColBlockBytes + (r0 + (u >> 3)) * 128 + (u & 7) * 16));
+    st_shared_zero16((cb ? sv1 : sv0) + uint32_t((r0 + (u >> 3)) * 128 + (u & 7) * 16));
   }
 }
 
@@ -406,8 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t sQ0 = sbase + C::kQ0, sQ1 = sbase + C::kQ1, sQ2 = sbase + C::kQ2, sP2 = sbase + C::kP2;
-  auto sK = [&](int st) { return sbase + C::kKV + st * C::kStageBytes; };
-  auto sV = [&](int st) { return sbase + C::kKV + st * C::kStageBytes + C::kTile; };
+  auto sK = [&](int st) { return sbase + uint32_t(C::k_off(st)); };
+  auto sV = [&](int st) { return sbase + uint32_t(C::v_off(st)); };    // V, column block 0
+  auto sV1 = [&](int st) { return sbase + uint32_t(C::v1_off(st)); };  // V, column block 1 (D = 128)
   const uint32_t bars = sbase + C::kBars;
   auto full_bar = [&](int st) { return bars + 8 * st; };
   auto empty_bar = [&](int st) { return bars + 8 * (S + st); };
@@ -500,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb) {
           ptx::tma_load_4d(sK(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page, full_bar(st));
-          ptx::tma_load_4d(sV(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page + 1,
+          ptx::tma_load_4d(cb ? sV1(st) : sV(st), &kv_map, cb * 64, head, start, 2 * cd.page + 1,
                            full_bar(st));
         }
         ++issued;
@@ -523,13 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool mine = (t < 2) ? (t < n_main) : has_tail;
     if (lane == 0 && mine) {
       const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sbase, 16, 1024) >> 32);
-      const uint32_t k0_lo = uint32_t(ptx::smem_desc_sw128(sK(0), 16, 1024));
+      auto k_lo_of = [&](int st) { return uint32_t(ptx::smem_desc_sw128(sK(st), 16, 1024)); };
       // V as an MN-major operand: the leading offset is the distance to the next 64-column
       // block (V's second half when D = 128, the ones block when the row sums ride along)
       auto v_lo_of = [&](int st) {
-        return uint32_t(ptx::smem_desc_sw128(sV(st), C::kOnes ? sOnes - sV(st) : kColBlockBytes, 1024));
+        return uint32_t(ptx::smem_desc_sw128(
+            sV(st), C::kSplitV ? sV1(st) - sV(st) : (C::kOnes ? sOnes - sV(st) : kColBlockBytes), 1024));
       };
-      constexpr uint32_t kStageStep = C::kStageBytes >> 4;       // 16-byte units
       constexpr uint32_t kHalfRows = (kHalfKeys * 128) >> 4;     // 64 key rows of a K or V column block
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
       ptx::tc_fence_after();
@@ -548,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             if (t == 0) trace<kDiag>(p, kTrFullSeen, c);
           }
-          const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep + uint32_t(g & 1) * kHalfRows;
+          const uint32_t k_lo = k_lo_of(st) + uint32_t(g & 1) * kHalfRows;
           const uint32_t tS = tmem + s_col<D>(t, g & 1);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
@@ -628,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = c % S;
           if (!ptx::mbar_wait_bounded(full_bar(st), (c / S) & 1, limit, abort_flag)) return false;
           ptx::tc_fence_after();
-          const uint32_t k_lo = k0_lo + uint32_t(st) * kStageStep;
+          const uint32_t k_lo = k_lo_of(st);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t aoff = uint32_t((k >> 2) * (kColBlockBytes >> 4) + (k & 3) * 2);
@@ -808,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (len < kHalfKeys * (b + 1)) {
           // ragged chunk: zero this half's V rows past the valid keys before the PV reads them
-          zero_v_rows<D>(sV((g >> 1) % S), max(len, kHalfKeys * b), kHalfKeys * (b + 1), r, 128);
+          zero_v_rows<D>(sV((g >> 1) % S), sV1((g >> 1) % S), max(len, kHalfKeys * b), kHalfKeys * (b + 1), r, 128);
           ptx::fence_proxy_async_smem();
         }
         ptx::tc_fence_before();
@@ -960,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_u16(p2_addr(p2, C::kP2ColBlock, rr, key), __bfloat16_as_ushort(pb));
           }
         }
-        if (len < kChunkTokens) zero_v_rows<D>(sV(j % S), len, kChunkTokens, tid, 128);
+        if (len < kChunkTokens) zero_v_rows<D>(sV(j % S), sV1(j % S), len, kChunkTokens, tid, 128);
         ptx::fence_proxy_async_smem();  // P2 stores (and zeroed V rows) -> visible to the tensor core
         ptx::tc_fence_before();
         long long t_arrive = 0;
