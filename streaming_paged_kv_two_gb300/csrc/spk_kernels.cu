@@ -222,6 +222,18 @@ __device__ __forceinline__ void load_f32_tile(const AttnParams& p, int head, con
   }
 }
 
+// c += a * b elementwise on a pair of floats, one packed instruction (fma.rn.f32x2)
+__device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%0, %1};\n\t"
+      "fma.rn.f32x2 z, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, z;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(const AttnParams p) {
   using C = F32Cfg<D>;
@@ -281,12 +293,13 @@ __global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(const AttnPa
     __syncthreads();
     const float* Ks = Ks_base + (2 * b) * C::kTileFloats;
     const float* Vs = Ks_base + (2 * b + 1) * C::kTileFloats;
-    // S = Q K^T for rows 4ty.. and keys tx + 16j
-    float s[4][4];
+    // S = Q K^T for rows 4ty.. and keys tx + 16j: each dot product accumulates its even
+    // and its odd dimensions in the two halves of a packed pair, added at the end
+    float s[4][4], se[4][4], so[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s[r][j] = 0.f;
+      for (int j = 0; j < 4; ++j) se[r][j] = so[r][j] = 0.f;
 #pragma unroll 4
     for (int d = 0; d < D; d += 4) {
       float4 q4[4], k4[4];
@@ -297,9 +310,15 @@ __global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(const AttnPa
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          s[r][j] = fmaf(q4[r].x, k4[j].x, fmaf(q4[r].y, k4[j].y, fmaf(q4[r].z, k4[j].z, fmaf(q4[r].w, k4[j].w, s[r][j]))));
+        for (int j = 0; j < 4; ++j) {
+          ffma2(se[r][j], so[r][j], q4[r].x, q4[r].y, k4[j].x, k4[j].y);
+          ffma2(se[r][j], so[r][j], q4[r].z, q4[r].w, k4[j].z, k4[j].w);
+        }
     }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[r][j] = se[r][j] + so[r][j];
     // online softmax over the tile's valid keys
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -337,11 +356,9 @@ __global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(const AttnPa
       for (int q = 0; q < kCols / 4; ++q) {
         const float4 v4 = *reinterpret_cast<const float4*>(Vs + j * C::kLd + tx * kCols + 4 * q);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          o[r][4 * q] = fmaf(pr[r], v4.x, o[r][4 * q]);
-          o[r][4 * q + 1] = fmaf(pr[r], v4.y, o[r][4 * q + 1]);
-          o[r][4 * q + 2] = fmaf(pr[r], v4.z, o[r][4 * q + 2]);
-          o[r][4 * q + 3] = fmaf(pr[r], v4.w, o[r][4 * q + 3]);
+        for (int r = 0; r < 4; ++r) {  // two columns per packed instruction
+          ffma2(o[r][4 * q], o[r][4 * q + 1], pr[r], pr[r], v4.x, v4.y);
+          ffma2(o[r][4 * q + 2], o[r][4 * q + 3], pr[r], pr[r], v4.z, v4.w);
         }
       }
     }
