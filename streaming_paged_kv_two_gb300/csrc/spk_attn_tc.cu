@@ -500,6 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent: the set-up above overlaps the previous kernel;
+  // Q, the pool and the outputs are touched only once that kernel (and with it
+  // everything before) has completed.  The plan tables read above come from a copy,
+  // which no launch overlaps.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the merge kernel that follows may be scheduled now; it waits for this grid to finish
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -1057,10 +1062,8 @@ cudaError_t launch_tc(const AttnParams& p, const CUtensorMap* map, cudaStream_t 
   const int64_t grid = int64_t(p.num_splits) * p.H * p.ngroups;
   if (grid <= 0 || grid > 0x7fffffff) return cudaErrorInvalidValue;
   if (p.trace != nullptr || p.dump_scores != nullptr)
-    attention_tc_kernel<D, true><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
-  else
-    attention_tc_kernel<D, false><<<unsigned(grid), kThreads, smem, s>>>(p, *map);
-  return cudaGetLastError();
+    return launch_dependent(attention_tc_kernel<D, true>, dim3(unsigned(grid)), dim3(kThreads), smem, s, p, *map);
+  return launch_dependent(attention_tc_kernel<D, false>, dim3(unsigned(grid)), dim3(kThreads), smem, s, p, *map);
 }
 
 }  // namespace

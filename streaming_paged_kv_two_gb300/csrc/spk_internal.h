@@ -138,6 +138,26 @@ struct MergeParams {
 };
 
 // Kernel launchers (defined in the .cu files).  All return the launch error.
+// Launch a kernel as a programmatic dependent of the previous kernel on the stream: its
+// grid may be scheduled before that kernel has finished, so it executes
+// griddepcontrol.wait before it touches memory that earlier work writes (the wait
+// returns at once when nothing earlier is running).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_append(const AppendParams& p, int elem_bytes, cudaStream_t s);
 cudaError_t launch_append_rope(const AppendRopeParams& p, int elem_bytes, cudaStream_t s);
 cudaError_t launch_attention_bf16(const AttnParams& p, const CUtensorMap* kv_map, cudaStream_t s);

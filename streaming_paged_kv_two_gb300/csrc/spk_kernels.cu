@@ -15,6 +15,10 @@ namespace spk {
 // Attention Outperforms SDPA Fallback in Streaming Inference", "Two-Stream
 // Design").  One thread moves 16 bytes; K and V in one launch.
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  // launched as a programmatic dependent: the previous kernel's writes (and everything
+  // before it) are visible once the wait returns; the next kernel may then be scheduled
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t upr = int32_t(p.row_bytes >> 4);  // 16-byte units per token row
   const int32_t per_kv = p.T * upr;
   const int32_t total = 2 * per_kv;
@@ -42,8 +46,7 @@ cudaError_t launch_append(const AppendParams& p, int /*elem_bytes*/, cudaStream_
   const int64_t units = 2 * int64_t(p.T) * (p.row_bytes >> 4);
   int64_t blocks = (units + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  append_kernel<<<int(blocks), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(append_kernel, dim3(unsigned(blocks)), dim3(256), 0, s, p);
 }
 
 // ------------------------------------------------------------------ merge
@@ -62,6 +65,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   // launched as a programmatic dependent of the attention kernel: wait until that grid
   // has completed and its partials are visible (returns at once otherwise)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int V = D / 4;  // float4 per row
   const int per_head = V * p.T;
   const int idx = int(blockIdx.x) * int(blockDim.x) + int(threadIdx.x);  // < B * H * V * T < 2^31 (host check)

@@ -80,6 +80,9 @@ __device__ __forceinline__ void rotate_store(const RowIo& io, int32_t u, uint4 x
 template <typename E>
 __global__ void __launch_bounds__(kRopeThreads) append_rope_kernel(const AppendRopeParams p) {
   __shared__ float2 cs[kMaxRopePairs];
+  // launched as a programmatic dependent (see append_kernel)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const AppendParams& a = p.a;
   const int32_t r = blockIdx.x;
   int32_t page, slot;
@@ -118,10 +121,8 @@ __global__ void __launch_bounds__(kRopeThreads) append_rope_kernel(const AppendR
 
 cudaError_t launch_append_rope(const AppendRopeParams& p, int elem_bytes, cudaStream_t s) {
   if (elem_bytes == 2)
-    append_rope_kernel<__nv_bfloat16><<<p.a.T, kRopeThreads, 0, s>>>(p);
-  else
-    append_rope_kernel<float><<<p.a.T, kRopeThreads, 0, s>>>(p);
-  return cudaGetLastError();
+    return launch_dependent(append_rope_kernel<__nv_bfloat16>, dim3(unsigned(p.a.T)), dim3(kRopeThreads), 0, s, p);
+  return launch_dependent(append_rope_kernel<float>, dim3(unsigned(p.a.T)), dim3(kRopeThreads), 0, s, p);
 }
 
 }  // namespace spk
