@@ -254,18 +254,6 @@ __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, f
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
-// acc + lo + hi, where lo and hi are the two bf16 halves of pk, added in fp32
-__device__ __forceinline__ float add_bf16x2_to(uint32_t pk, float acc) {
-  float d;
-  asm("{\n\t.reg .b16 lo, hi;\n\t"
-      "mov.b32 {lo, hi}, %1;\n\t"
-      "add.rn.f32.bf16 %0, lo, %2;\n\t"
-      "add.rn.f32.bf16 %0, hi, %0;\n\t}"
-      : "=f"(d)
-      : "r"(pk), "f"(acc));
-  return d;
-}
-
 // 2^x of a packed pair of bf16 values, result a packed pair of bf16
 __device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
   uint32_t y;

@@ -45,13 +45,15 @@
 //               head_dim 128 issues Q K^T of half g+1 once the softmax has released
 //               the S buffer.  The consumers advance independently; a K/V stage is
 //               released once every consumer is done with it.
-// head_dim 64: Q_t is the TMEM A operand of Q K^T (only K is read from shared memory),
-// and the PV MMA's B operand is V extended by a 16-column block of ones in shared
-// memory, so O0/O1 are 80 columns wide and column 64 accumulates the row sum of the bf16
-// P that the MMA consumed.  TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) |
-// O0 | O1 (80 each) | Q0 | Q1 (32 each) | S2^T (16) | O2^T (8).
-// head_dim 128: Q in shared memory; S0 | S1 | P0 | P1 | O0 | O1 (128 each) | S2^T (16) |
-// O2^T (16); fp32 row sums.
+// The PV MMA's B operand is V extended by a 16-column block of ones in shared memory, so
+// O0/O1 are D + 16 columns wide and column D accumulates the row sum of the bf16 P that
+// the MMA consumed.
+// head_dim 64: Q_t is the TMEM A operand of Q K^T (only K is read from shared memory).
+// TMEM (512 columns): S0[0] | S0[1] | S1[0] | S1[1] (64 each) | O0 | O1 (80 each) |
+// Q0 | Q1 (32 each) | S2^T (16) | O2^T (8).
+// head_dim 128: Q in shared memory; S0 | S1 (64 each) | P0 | P1 (32 each) | O0 | O1
+// (144 each) | S2^T (16) | O2^T (16), all 512 columns; V's two column blocks and the
+// ones block sit at one stride per stage (Cfg's split-V layout).
 // Key rows past a ragged chunk's length are zeroed in the V tile before a PV MMA reads
 // them, so whatever a slot past the valid tokens holds (a rolled-back frame, an earlier
 // stream) cannot reach the output, not even as 0 * Inf.
@@ -96,7 +98,6 @@ struct Cfg {
   static constexpr int kQ2ColBlock = kTailN * 128;    // one 64-dim column block of the tail Q tile
   // the row sums come out of the PV MMA, whose B operand is V extended by a 16-column
   // block of ones (O gets 16 more columns, each holding the row sum)
-  static constexpr bool kOnes = true;
   // D == 128: V has two column blocks, so the ones block must be the third at the same
   // stride (the MMA's leading offset) from each stage's V: each stage puts its second V
   // block halfway between its first and the one shared ones block (see the layout below)
@@ -117,7 +118,7 @@ struct Cfg {
   // stage 1 (7), K of stage 0 (8-9), V1 of stage 1 (10), V0 of stage 0 (11), V1 of stage 0
   // (12), ones (13): stage 0's V blocks and the ones block are 1 block apart, stage 1's 3
   static constexpr int kOnesBlk = kSplitV ? 13 * kColBlockBytes : kKV + kStages * kStageBytes;  // 128 rows x 64 bf16 ones
-  static constexpr int kTailX = kOnesBlk + (kOnes ? kColBlockBytes : 0);
+  static constexpr int kTailX = kOnesBlk + kColBlockBytes;
   // K tile, V column block 0 and V column block 1 of stage st (byte offsets)
   __host__ __device__ static constexpr int k_off(int st) {
     return kSplitV ? (st ? 5 : 8) * kColBlockBytes : kKV + st * kStageBytes;
@@ -135,7 +136,7 @@ struct Cfg {
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
-  static constexpr int kOW = D + (kOnes ? 16 : 0);  // TMEM columns of a main tile's O
+  static constexpr int kOW = D + 16;  // TMEM columns of a main tile's O (the last 16: row sums)
   // D == 64: S_t[b] at 64 (2t + b), P over S; D == 128: S_t at 64 t, P_t at kP0 + 32 t
   static constexpr uint32_t kP0 = 2 * kHalfKeys;
   static constexpr uint32_t kO0 = kEarly ? kP0 + kHalfKeys : 4 * kHalfKeys, kO1 = kO0 + kOW;
@@ -247,28 +248,20 @@ __device__ __forceinline__ void store_q_row(uint32_t sq, int r, const uint4* src
 }
 
 // p = 2^(s*sl2 - m) for the 64 fp32 scores of a half chunk (two 32-column quarters),
-// packed to bf16 pairs in pk.  kSum: fp32 exponentials, one rounding, and the fp32 sum
-// of the rounded values is returned; otherwise exponentials of the bf16-rounded
-// argument pairs (the row sums come from the PV MMA) and 0 is returned.  *orr receives
-// the OR of the packed words (their high exponent bits flag a value >= 2).
-template <bool kSum>
-__device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* sb, float sl2, float neg_m,
-                                            uint32_t (&pk)[32], uint32_t* orr) {
-  float sum[4] = {0.f, 0.f, 0.f, 0.f};
+// as exponentials of the bf16-rounded argument pairs packed to bf16 pairs in pk (the row
+// sums come from the PV MMA).  *orr receives the OR of the packed words (their high
+// exponent bits flag a value >= 2).
+__device__ __forceinline__ void exp_pack64(const uint32_t* sa, const uint32_t* sb, float sl2, float neg_m,
+                                           uint32_t (&pk)[32], uint32_t* orr) {
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const uint32_t* s = e < 16 ? sa : sb;
     const int i = 2 * (e & 15);
     float x0, x1;
     ptx::fma2(x0, x1, __uint_as_float(s[i]), __uint_as_float(s[i + 1]), sl2, neg_m);
-    if constexpr (kSum) {
-      pk[e] = pack_bf16(ptx::ex2(x0), ptx::ex2(x1));
-      sum[e & 3] = ptx::add_bf16x2_to(pk[e], sum[e & 3]);
-    } else {
-      // x < 1 unless the max moves, so the argument's bf16 rounding moves p by at most
-      // 0.14 % (at x = 1), below P's own rounding
-      pk[e] = ptx::ex2_bf16x2(pack_bf16(x0, x1));
-    }
+    // x < 1 unless the max moves, so the argument's bf16 rounding moves p by at most
+    // 0.14 % (at x = 1), below P's own rounding
+    pk[e] = ptx::ex2_bf16x2(pack_bf16(x0, x1));
   }
   uint32_t o0 = 0, o1 = 0;
 #pragma unroll
@@ -277,7 +270,6 @@ __device__ __forceinline__ float exp_pack64(const uint32_t* sa, const uint32_t* 
     o1 = or3(o1, pk[e + 2], pk[e + 3]);
   }
   *orr = o0 | o1;
-  return (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
 
 // max over 32 scores (three-input max: two new values per instruction)
@@ -324,14 +316,12 @@ __device__ __forceinline__ void rescale_tmem(uint32_t taddr, int ncols, float co
 // row that did (`need`) moves its running max m to max(m, the half's max); O (every
 // earlier PV of this tile: when o_cols > 0, wait for the previous half's PV, tracked by
 // pv_bar) is scaled by corr = 2^(m - m_new), and the half's P is recomputed with the new
-// offset.  Returns (m_new, sum of the new rounded P when kSum, corr, 1 if the wait
-// succeeded else 0).
+// offset.  Returns (m_new, 1 if the wait succeeded else 0).
 //
 // head_dim 64: the scores are still in TMEM (the S buffer is not released before P is
 // stored over it), so this path reloads them and stores P itself; kept out of line so
 // the hot loop's registers are not spent on it.
-template <bool kSum>
-__device__ __noinline__ float4 move_running_max_tmem(uint32_t tO, uint32_t tS, int o_cols, bool need, float m,
+__device__ __noinline__ float2 move_running_max_tmem(uint32_t tO, uint32_t tS, int o_cols, bool need, float m,
                                                      float sl2, int first_key, int len, uint32_t pv_bar,
                                                      uint32_t parity, long long limit, const volatile int* abort_flag) {
   uint32_t sa[32], sb[32], pk[32], orr;
@@ -349,17 +339,16 @@ __device__ __noinline__ float4 move_running_max_tmem(uint32_t tO, uint32_t tS, i
     ptx::tc_fence_after();
     rescale_tmem(tO, o_cols, corr);
   }
-  const float sum = exp_pack64<kSum>(sa, sb, sl2, -m_new, pk, &orr);
+  exp_pack64(sa, sb, sl2, -m_new, pk, &orr);
   ptx::tmem_st32(tS, pk);
   ptx::tmem_wait_st();
-  return make_float4(m_new, sum, corr, ok ? 1.f : 0.f);
+  return make_float2(m_new, ok ? 1.f : 0.f);
 }
 
 // head_dim 128: the S buffer has been released, so the path works on the (masked)
 // scores held in registers and leaves the new P in pk; inlined, because an out-of-line
 // call would put those arrays in local memory for the whole loop.
-template <bool kSum>
-__device__ __forceinline__ float4 move_running_max_regs(const uint32_t (&sa)[32], const uint32_t (&sb)[32],
+__device__ __forceinline__ float2 move_running_max_regs(const uint32_t (&sa)[32], const uint32_t (&sb)[32],
                                                         uint32_t (&pk)[32], uint32_t tO, int o_cols, bool need,
                                                         float m, float sl2, uint32_t pv_bar, uint32_t parity,
                                                         long long limit, const volatile int* abort_flag) {
@@ -373,8 +362,8 @@ __device__ __forceinline__ float4 move_running_max_regs(const uint32_t (&sa)[32]
     rescale_tmem(tO, o_cols, corr);
   }
   uint32_t orr;
-  const float sum = exp_pack64<kSum>(sa, sb, sl2, -m_new, pk, &orr);
-  return make_float4(m_new, sum, corr, ok ? 1.f : 0.f);
+  exp_pack64(sa, sb, sl2, -m_new, pk, &orr);
+  return make_float2(m_new, ok ? 1.f : 0.f);
 }
 
 // Write 32 columns [col0, col0+32) of one output row from raw fp32 TMEM values times
@@ -552,10 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t hi = uint32_t(ptx::smem_desc_sw128(sbase, 16, 1024) >> 32);
       auto k_lo_of = [&](int st) { return uint32_t(ptx::smem_desc_sw128(sK(st), 16, 1024)); };
       // V as an MN-major operand: the leading offset is the distance to the next 64-column
-      // block (V's second half when D = 128, the ones block when the row sums ride along)
+      // block (D = 64: the ones block; D = 128: V's second block, the ones block one more
+      // stride on)
       auto v_lo_of = [&](int st) {
-        return uint32_t(ptx::smem_desc_sw128(
-            sV(st), C::kSplitV ? sV1(st) - sV(st) : (C::kOnes ? sOnes - sV(st) : kColBlockBytes), 1024));
+        return uint32_t(ptx::smem_desc_sw128(sV(st), C::kSplitV ? sV1(st) - sV(st) : sOnes - sV(st), 1024));
       };
       constexpr uint32_t kHalfRows = (kHalfKeys * 128) >> 4;     // 64 key rows of a K or V column block
       bool ok = ptx::mbar_wait_bounded(q_full, 0, limit, abort_flag);
@@ -728,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_q_row<D>(t ? sQ1 : sQ0, r, qsrc, row_ok);
       }
     }
-    if constexpr (C::kOnes) {  // the ones block: 16 KB over the 256 main-softmax threads
+    {  // the ones block: 16 KB over the 256 main-softmax threads
       const uint32_t ones = 0x3F803F80u;  // two bf16 1.0
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -762,7 +751,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (tile_on) {
       float m = -INFINITY;  // running max of scaled logits (log2 units); the first half sets it
-      float l = 0.f;        // D = 128: running sum of the bf16-rounded P (D = 64 takes it from O)
       bool ok = true;
       int len = 0;
       int len_next = n > 0 ? (__ldg(&p.chunks[c0].start_len) >> 16) : 0;
@@ -795,29 +783,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           mask32(sa, kHalfKeys * b, len);
           mask32(sb, kHalfKeys * b + 32, len);
           uint32_t orr;
-          const float ps = exp_pack64<!C::kOnes>(sa, sb, sl2, -m, pk, &orr);
+          exp_pack64(sa, sb, sl2, -m, pk, &orr);
           const bool need = (orr & kPHighBits) != 0;
           if (__any_sync(0xffffffffu, need)) {
-            float4 r4;
+            float2 r2;
             if constexpr (kEarly) {
-              r4 = move_running_max_regs<!C::kOnes>(sa, sb, pk, tO, g > 0 ? C::kOW : 0, need, m, sl2, pv_done(t),
-                                                    uint32_t(g - 1) & 1u, limit, abort_flag);
+              r2 = move_running_max_regs(sa, sb, pk, tO, g > 0 ? C::kOW : 0, need, m, sl2, pv_done(t),
+                                         uint32_t(g - 1) & 1u, limit, abort_flag);
             } else {
-              r4 = move_running_max_tmem<!C::kOnes>(tO, tS, g > 0 ? C::kOW : 0, need, m, sl2, kHalfKeys * b, len,
-                                                    pv_done(t), uint32_t(g - 1) & 1u, limit, abort_flag);
+              r2 = move_running_max_tmem(tO, tS, g > 0 ? C::kOW : 0, need, m, sl2, kHalfKeys * b, len, pv_done(t),
+                                         uint32_t(g - 1) & 1u, limit, abort_flag);
               p_stored = true;
             }
-            if constexpr (!C::kOnes) l = l * r4.z + r4.y;
-            m = r4.x;
+            m = r2.x;
             waited_pv = true;
             if constexpr (kDiag)  // diagnostics: count rescales of an accumulated O (any CTA)
               if (p.trace != nullptr && g > 0 && lane == 0) atomicAdd(p.trace + int64_t(kTraceEvents) * p.trace_cap, 1ull);
-            if (r4.w == 0.f) {
+            if (r2.y == 0.f) {
               ok = false;
               break;
             }
-          } else {
-            if constexpr (!C::kOnes) l += ps;
           }
           if (!kEarly && !p_stored) {  // P over the scores it came from
             ptx::tmem_st32(tS, pk);
@@ -849,12 +834,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) signal_abort(p.status, abort_flag);
       if (ok && ptx::mbar_wait_warp(o_done(t), 0, limit, abort_flag) && warp_on) {
         ptx::tc_fence_after();
-        if constexpr (C::kOnes) {  // the row sum, as accumulated by the PV MMA
-          uint32_t lv[16];
-          ptx::tmem_ld16(tO + D, lv);
-          ptx::tmem_wait_ld();
-          l = __uint_as_float(lv[0]);
-        }
+        uint32_t lv[16];  // the row sum, as accumulated by the PV MMA
+        ptx::tmem_ld16(tO + D, lv);
+        ptx::tmem_wait_ld();
+        const float l = __uint_as_float(lv[0]);
         const float inv_l = 1.f / l;
 #pragma unroll 1
         for (int j = 0; j < D / 32; ++j) {
