@@ -448,70 +448,86 @@ def run_gpu(args, w: wl.Workload):
     append_ms = [a.elapsed_time(b) for a, b in ev_app]
 
     # ------------------------------------------------ e2e: host buffers, copies in the timed region
-    # Every step copies its q/k/v from pinned host memory and its outputs back.  The
-    # copies run on their own streams (host->device, device->host) so block b+1's inputs
-    # move while block b computes; events order each copy against the compute stream.
-    hq = [[qcat[vi][b].cpu().pin_memory() for b in range(L)] for vi in range(NV)]
-    hkv = [[[tuple(x.cpu().pin_memory() for x in kvs[vi][s][b]) for b in range(L)] for s in range(B)]
-           for vi in range(NV)]
-    dq = [[torch.empty_like(qcat[0][b]) for b in range(L)] for _ in range(2)]          # [set][block]
-    dkv = [[[tuple(torch.empty_like(x) for x in kvs[0][s][b]) for b in range(L)] for s in range(B)]
-           for _ in range(2)]                                                            # [set][stream][block]
-    hout = [torch.empty(outs[b].shape, dtype=outs[b].dtype).pin_memory() for b in range(L)]
+    # Every step copies its q/k/v from pinned host memory and its outputs back.  A step's
+    # inputs sit in one pinned host buffer (per frame variant: q of each block, then k and
+    # v of each (stream, block)) and go to the device in one copy; its outputs come back
+    # in one copy.  The copies run on their own streams and the device sets are double
+    # buffered, so step f+1's inputs move while step f computes; events order each copy
+    # against the compute stream.  Step f+1's input copy starts once step f's plan is
+    # uploaded: the plan upload is itself a host->device copy on the compute stream and
+    # would otherwise queue behind the larger input copy.
+    q_elems = [qcat[0][b].numel() for b in range(L)]
+    kv_elems = T * w.num_heads * w.head_dim
+    per_block = q_elems[0] + 2 * B * kv_elems
+    hin = []
+    for vi in range(NV):
+        parts = []
+        for b in range(L):
+            parts.append(qcat[vi][b].reshape(-1))
+            for s in range(B):
+                parts += [kvs[vi][s][b][0].reshape(-1), kvs[vi][s][b][1].reshape(-1)]
+        hin.append(torch.cat(parts).cpu().pin_memory())
+    din = [torch.empty_like(hin[0], device=dev) for _ in range(2)]
+
+    def in_views(st):
+        buf, dq, dkv = din[st], [], [[None] * L for _ in range(B)]
+        for b in range(L):
+            o = b * per_block
+            dq.append(buf[o:o + q_elems[b]].view(qcat[0][b].shape))
+            o += q_elems[b]
+            for s in range(B):
+                dkv[s][b] = (buf[o:o + kv_elems].view(kvs[0][s][b][0].shape),
+                             buf[o + kv_elems:o + 2 * kv_elems].view(kvs[0][s][b][1].shape))
+                o += 2 * kv_elems
+        return dq, dkv
+
+    views = [in_views(0), in_views(1)]
+    dout = [torch.empty((L,) + tuple(outs[0].shape), dtype=outs[0].dtype, device=dev) for _ in range(2)]
+    hout = torch.empty(dout[0].shape, dtype=dout[0].dtype).pin_memory()
     hpos = pos_all.cpu().pin_memory() if args.rope else None          # [frame, T, 3]
     dpos = [torch.empty_like(pos_all[0]) for _ in range(2)] if args.rope else None
-    ev_pos = [None, None]                   # the last append that read dpos[set] is done
-    h2d = sum(x.numel() * x.element_size() for b in range(L) for x in (hq[0][b],)) + \
-        sum(x.numel() * x.element_size() for s in range(B) for b in range(L) for x in hkv[0][s][b]) + \
-        (hpos[0].numel() * hpos[0].element_size() if args.rope else 0)
-    d2h = sum(x.numel() * x.element_size() for x in hout)
+    h2d = hin[0].numel() * hin[0].element_size() + (hpos[0].numel() * hpos[0].element_size() if args.rope else 0)
+    d2h = hout.numel() * hout.element_size()
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [[torch.cuda.Event() for _ in range(L)] for _ in range(2)]      # inputs of (set, block) landed
-    ev_used = [[None] * L for _ in range(2)]                                # compute done with (set, block)
-    ev_out = [torch.cuda.Event() for _ in range(L)]                         # out[b] written
-    ev_back = [None] * L                                                    # out[b] copied to the host
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of set st landed
+    ev_planned = torch.cuda.Event()                     # the last step's plan is uploaded (and the step
+    planned = [False]                                   # before it is done with its inputs)
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # dout[st] written
+    ev_back = [None, None]                              # dout[st] copied to the host
 
     def e2e_step(f):
         vi, st = f % NV, f % 2
+        dq, dkv = views[st]
         with torch.cuda.stream(up):
+            if planned[0]:
+                up.wait_event(ev_planned)
+            din[st].copy_(hin[vi], non_blocking=True)
             if args.rope:
-                if ev_pos[st] is not None:
-                    up.wait_event(ev_pos[st])
                 dpos[st].copy_(hpos[f], non_blocking=True)
-            for b in range(L):
-                if ev_used[st][b] is not None:
-                    up.wait_event(ev_used[st][b])
-                dq[st][b].copy_(hq[vi][b], non_blocking=True)
-                for s in range(B):
-                    dkv[st][s][b][0].copy_(hkv[vi][s][b][0], non_blocking=True)
-                    dkv[st][s][b][1].copy_(hkv[vi][s][b][1], non_blocking=True)
-                ev_in[st][b].record(up)
-        stream.wait_event(ev_in[st][0])
+            ev_in[st].record(up)
+        stream.wait_event(ev_in[st])
+        if ev_back[st] is not None:
+            stream.wait_event(ev_back[st])           # step f-2's copy of dout[st] is done
         for s in range(B):
-            append_one(f, s, 0, dkv[st][s][0][0], dkv[st][s][0][1], q=dq[st][0][s * T:(s + 1) * T],
+            append_one(f, s, 0, dkv[s][0][0], dkv[s][0][1], q=dq[0][s * T:(s + 1) * T],
                        pos=dpos[st] if args.rope else None)
         for s in range(B):
             cache.evict_frames(s)
         cache.plan(ws, stream)
+        ev_planned.record(stream)
+        planned[0] = True
         for b in range(L):
             if b:
-                stream.wait_event(ev_in[st][b])
                 for s in range(B):
-                    append_one(f, s, b, dkv[st][s][b][0], dkv[st][s][b][1], q=dq[st][b][s * T:(s + 1) * T],
+                    append_one(f, s, b, dkv[s][b][0], dkv[s][b][1], q=dq[b][s * T:(s + 1) * T],
                                pos=dpos[st] if args.rope else None)
-            if ev_back[b] is not None:
-                stream.wait_event(ev_back[b])       # the previous step's copy of out[b] is done
-            if args.rope and b == L - 1:
-                ev_pos[st] = torch.cuda.Event()
-                ev_pos[st].record(stream)
-            cache.run_attention(b, qrot[b] if args.rope else dq[st][b], outs[b], ws, stream)
-            ev_out[b].record(stream)
-            ev_used[st][b] = ev_out[b]
-            with torch.cuda.stream(down):
-                down.wait_event(ev_out[b])
-                hout[b].copy_(outs[b], non_blocking=True)
-                ev_back[b] = torch.cuda.Event()
-                ev_back[b].record(down)
+            cache.run_attention(b, qrot[b] if args.rope else dq[b], dout[st][b], ws, stream)
+        ev_out[st].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_out[st])
+            hout.copy_(dout[st], non_blocking=True)
+            ev_back[st] = torch.cuda.Event()
+            ev_back[st].record(down)
 
     for _ in range(2):
         e2e_step(f)
@@ -526,8 +542,8 @@ def run_gpu(args, w: wl.Workload):
     for _ in range(K):
         e2e_step(f)
         f += 1
-    for b in range(L):
-        stream.wait_event(ev_back[b])              # every output is back on the host
+    for st in range(2):
+        stream.wait_event(ev_back[st])             # every output is back on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1000.0, device=dev)
