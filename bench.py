@@ -547,6 +547,20 @@ def run_gpu(args, w: wl.Workload):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_elapsed = reduce_max(e0.elapsed_time(e1) / 1000.0, device=dev)
+    # untimed check: the last e2e step's outputs, as copied back to the host, equal the
+    # same frame's attention from the device-resident q (same plan, same kernels, so bit
+    # for bit); with --rope q is produced by the appends themselves, so there is no
+    # device-resident q to rerun from
+    e2e_match = None
+    if not args.rope:
+        vi_last = (f - 1) % NV
+        chk = torch.empty_like(outs[0])
+        bits = torch.int16 if chk.element_size() == 2 else torch.int32
+        e2e_match = True
+        for b in range(L):
+            cache.run_attention(b, qcat[vi_last][b], chk, ws, stream)
+            torch.cuda.synchronize()
+            e2e_match = e2e_match and bool(torch.equal(chk.cpu().view(bits), hout[b].view(bits)))
 
     # ------------------------------------------------ report
     hbm, tflops, tflops_sus, peak_kind = load_peaks()
@@ -593,7 +607,7 @@ def run_gpu(args, w: wl.Workload):
         "roofline_frame_steps_per_s": 1.0 / (t_roof_block * L),
         "e2e": {"value": aggregate_throughput(K, world, e2e_elapsed), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "frames": [f - K + 1, f]},
+                "frames": [f - K + 1, f], "outputs_match_device_path": e2e_match},
         "append": {"kernel": "append_rope_kernel" if args.rope else "append_kernel",
                    "avg_launch_us": statistics.mean(append_ms) * 1e3,
                    "bytes_per_launch": append_bytes,
