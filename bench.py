@@ -620,19 +620,54 @@ def run_gpu(args, w: wl.Workload):
         "device_status": status,
         "fast_forward_s": t_ff,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        reps = 50
-        times, cpu_value = oracle_block_sample(w.replace(frames=f_first + K + reps + 4), f_first + K, heads=2,
-                                               reps=reps, budget_s=20.0)
-        line["cpu_baseline"] = {
-            "value": cpu_value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"{len(times)} reps of one frame of bookkeeping + gather + fp64 attention of block 0 over 2 "
-                       f"of {w.num_heads} heads at frame {f_first + K}; extrapolated to all heads and "
-                       f"{w.num_blocks} blocks")}
-    if rank == 0:
-        print(json.dumps(line))
     cache.close()
-    return 0
+    return line if rank == 0 else None
+
+
+def add_cpu_baseline(line: dict, w: wl.Workload) -> None:
+    """The fp64 oracle timed on the host cores on a bounded sample of the same workload
+    (run after every GPU timing of the process, so that its host threads cannot slow a
+    launching thread)."""
+    reps = 50
+    frame = line["config"]["timed_frames"][1]
+    times, cpu_value = oracle_block_sample(w.replace(frames=frame + reps + 4), frame, heads=2, reps=reps,
+                                           budget_s=20.0)
+    line["cpu_baseline"] = {
+        "value": cpu_value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+        "sample": (f"{len(times)} reps of one frame of bookkeeping + gather + fp64 attention of block 0 over 2 "
+                   f"of {w.num_heads} heads at frame {frame}; extrapolated to all heads and "
+                   f"{w.num_blocks} blocks")}
+
+
+SECONDARY = ("lingbot_like_200", "high_res_999", "batched4_d128")
+
+
+def run_secondary(args) -> list:
+    """The other streaming workloads, timed briefly in the same run after the headline
+    line (20 frame-steps each, device-resident and end to end), so that one default run
+    records every workload's throughput and roofline fraction.  A workload that fails
+    is reported with its error instead."""
+    import torch
+    out = []
+    for name in SECONDARY:
+        sub = argparse.Namespace(**vars(args))
+        sub.workload, sub.steps, sub.warmup, sub.no_cpu_baseline = name, 20, 5, True
+        torch.cuda.empty_cache()
+        try:
+            d = run_gpu(sub, wl.CONFIGS[name])
+        except Exception as e:  # noqa: BLE001 - the headline line must still print
+            out.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
+            continue
+        r = d["roofline"]
+        out.append({
+            "workload": name, "value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+            "steps": d["steps"], "warmup": d["warmup"], "dtype": d["dtype"],
+            "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "avg_launch_us",
+                                           "frac_of_sustained") if k in r},
+            "e2e": {"value": d["e2e"]["value"], "outputs_match_device_path": d["e2e"]["outputs_match_device_path"]},
+            "gpu_launches": d["gpu_launches"], "clocks": d["clocks"], "device_status": d["device_status"]})
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- scale-phase prefill
@@ -745,6 +780,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="spk", choices=["spk", "reference"])
     ap.add_argument("--ref-heads", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the brief runs of the other workloads that the plain default run appends")
     ap.add_argument("--rope", action="store_true",
                     help="streaming step: append through the fused 3-D rotary scatter (q and k turned)")
     ap.add_argument("--splits", type=int, default=0,
@@ -768,7 +805,16 @@ def main(argv=None):
         return run_reference(args, w)
     if args.query_frames > 1:
         return run_prefill(args, w)
-    return run_gpu(args, w)
+    line = run_gpu(args, w)
+    if line is not None:
+        plain_default = (args.workload == "steady_state_10k" and not (args.rope or args.f32 or args.blocks or args.splits)
+                         and line["n_gpus"] == 1)
+        if plain_default and not args.no_secondary:
+            line["secondary"] = run_secondary(args)
+        if line["n_gpus"] == 1 and not args.no_cpu_baseline:
+            add_cpu_baseline(line, w)
+        print(json.dumps(line))
+    return 0
 
 
 if __name__ == "__main__":
