@@ -639,33 +639,44 @@ def add_cpu_baseline(line: dict, w: wl.Workload) -> None:
                    f"{w.num_blocks} blocks")}
 
 
-SECONDARY = ("lingbot_like_200", "high_res_999", "batched4_d128")
+# (workload, variant, steps): the other streaming workloads, then the fp32 accuracy
+# path, the fused rotary append and the scale-phase prefill
+SECONDARY = (("lingbot_like_200", "", 20), ("high_res_999", "", 20), ("batched4_d128", "", 20),
+             ("lingbot_like_200", "f32", 5), ("steady_state_10k", "rope", 20),
+             ("steady_state_10k", "prefill8", 20))
 
 
 def run_secondary(args) -> list:
-    """The other streaming workloads, timed briefly in the same run after the headline
-    line (20 frame-steps each, device-resident and end to end), so that one default run
-    records every workload's throughput and roofline fraction.  A workload that fails
-    is reported with its error instead."""
+    """The other workloads and paths, timed briefly in the same run after the headline
+    line (device-resident and, for the streaming steps, end to end), so that one default
+    run records every workload's throughput and roofline fraction.  A workload that
+    fails is reported with its error instead."""
     import torch
     out = []
-    for name in SECONDARY:
+    for name, variant, steps in SECONDARY:
         sub = argparse.Namespace(**vars(args))
-        sub.workload, sub.steps, sub.warmup, sub.no_cpu_baseline = name, 20, 5, True
+        sub.workload, sub.steps, sub.warmup, sub.no_cpu_baseline = name, steps, 5 if steps >= 20 else 3, True
+        sub.f32, sub.rope, sub.query_frames = variant == "f32", variant == "rope", 8 if variant == "prefill8" else 1
+        w = wl.CONFIGS[name]
+        if sub.f32:
+            w = w.replace(dtype="f32", name=f"{w.name}_f32")
         torch.cuda.empty_cache()
         try:
-            d = run_gpu(sub, wl.CONFIGS[name])
+            d = run_prefill(sub, w) if sub.query_frames > 1 else run_gpu(sub, w)
         except Exception as e:  # noqa: BLE001 - the headline line must still print
-            out.append({"workload": name, "error": f"{type(e).__name__}: {e}"})
+            out.append({"workload": name, "variant": variant, "error": f"{type(e).__name__}: {e}"})
             continue
         r = d["roofline"]
-        out.append({
-            "workload": name, "value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
-            "steps": d["steps"], "warmup": d["warmup"], "dtype": d["dtype"],
+        entry = {
+            "workload": name, "variant": variant, "metric": d["metric"], "value": d["value"], "unit": d["unit"],
+            "ms_per_step": d["ms_per_step"], "steps": d["steps"], "warmup": d["warmup"], "dtype": d["dtype"],
             "roofline": {k: r[k] for k in ("bound", "achieved", "peak", "unit", "frac", "avg_launch_us",
                                            "frac_of_sustained") if k in r},
-            "e2e": {"value": d["e2e"]["value"], "outputs_match_device_path": d["e2e"]["outputs_match_device_path"]},
-            "gpu_launches": d["gpu_launches"], "clocks": d["clocks"], "device_status": d["device_status"]})
+            "gpu_launches": d["gpu_launches"], "clocks": d["clocks"], "device_status": d["device_status"]}
+        if "e2e" in d:
+            entry["e2e"] = {"value": d["e2e"]["value"],
+                            "outputs_match_device_path": d["e2e"]["outputs_match_device_path"]}
+        out.append(entry)
     torch.cuda.empty_cache()
     return out
 
@@ -765,10 +776,8 @@ def run_prefill(args, w: wl.Workload):
         "gpu_launches": (F * B * L + L * (2 if info["merge_needed"] else 1)) * K,
         "plan": info, "clocks": clk, "device_status": status,
     }
-    if rank == 0:
-        print(json.dumps(line))
     cache.close()
-    return 0
+    return line if rank == 0 else None
 
 
 def main(argv=None):
@@ -804,7 +813,10 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args, w)
     if args.query_frames > 1:
-        return run_prefill(args, w)
+        line = run_prefill(args, w)
+        if line is not None:
+            print(json.dumps(line))
+        return 0
     line = run_gpu(args, w)
     if line is not None:
         plain_default = (args.workload == "steady_state_10k" and not (args.rope or args.f32 or args.blocks or args.splits)
