@@ -131,8 +131,9 @@ struct Cfg {
   }  // tail exchange: [2][4][8] maxima, [2][4] flags
   static constexpr int kBars = kTailX + (kTail ? 2 * 4 * (kTailMaxRows + 1) * 4 + 32 : 0);
   // full[S], empty[S], q_full, s_full[2][2], s_free[2], p_ready[2][2], pv_done[2], o_done[3],
-  // s2_full, s2_free, p2_ready[2], pv2_done
-  static constexpr int kNumBars = 2 * kStages + 21;
+  // s2_full, s2_free, p2_ready[2], pv2_done; D == 128 also v_full[S], v_empty[S] (full/empty
+  // then track K only)
+  static constexpr int kNumBars = 2 * kStages + 21 + (kSplitV ? 2 * kStages : 0);
   static constexpr int kMisc = kBars + 8 * kNumBars;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kLaunch = kBytes + 1024;  // slack for 1024-byte alignment
@@ -432,6 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s2_full = q_full + 8 * 16, s2_free = q_full + 8 * 17;
   auto p2_ready = [&](int b) { return q_full + 8 * (18 + b); };
   const uint32_t pv2_done = q_full + 8 * 20;
+  // head_dim 128: K and V of a stage land and are released separately.  K is read only
+  // by the chunk's Q K^T (and the tail's S2^T), V until its last PV, so the next chunk's K
+  // can be requested about a period earlier than the stage as a whole; with two stages
+  // that had bound the chunk period.
+  constexpr bool kSplitKV = C::kSplitV;
+  auto v_full = [&](int st) { return kSplitKV ? q_full + 8 * (21 + st) : full_bar(st); };
+  auto v_empty = [&](int st) { return kSplitKV ? q_full + 8 * (21 + S + st) : empty_bar(st); };
   constexpr bool kEarly = C::kEarly;
   const uint32_t sOnes = sbase + C::kOnesBlk;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
@@ -462,6 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(full_bar(i), 1);
       ptx::mbar_init(empty_bar(i), ncons);  // one release per consumer of the chunk
+      if (kSplitKV) {
+        ptx::mbar_init(v_full(i), 1);
+        ptx::mbar_init(v_empty(i), ncons);
+      }
     }
     ptx::mbar_init(q_full, kSoftmaxThreads);
     for (int t = 0; t < 2; ++t) {
@@ -502,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       ptx::prefetch_tmap(&kv_map);
       int issued = 0;
+      bool k_only_last = false;
       const int nload = dump ? min(n, 1) : n;
       for (int i = 0; i < nload; ++i) {
         const int st = i % S;
@@ -511,18 +524,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const ChunkDesc cd = p.chunks[c0 + i];
         const int start = cd.start_len & 0xFFFF;
-        ptx::mbar_arrive_expect_tx(full_bar(st), 2 * C::kTile);
+        ptx::mbar_arrive_expect_tx(full_bar(st), (kSplitKV ? 1 : 2) * C::kTile);
         trace<kDiag>(p, kTrTmaIssue, i);
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) {
+        for (int cb = 0; cb < D / 64; ++cb)
           ptx::tma_load_4d(sK(st) + cb * kColBlockBytes, &kv_map, cb * 64, head, start, 2 * cd.page, full_bar(st));
-          ptx::tma_load_4d(cb ? sV1(st) : sV(st), &kv_map, cb * 64, head, start, 2 * cd.page + 1,
-                           full_bar(st));
+        bool v_ok = true;
+        if (kSplitKV) {  // V once the stage's previous V is released
+          v_ok = ptx::mbar_wait_bounded(v_empty(st), ((i / S) & 1) ^ 1, limit, abort_flag);
+          if (v_ok) ptx::mbar_arrive_expect_tx(v_full(st), C::kTile);
+        }
+        if (v_ok) {
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            ptx::tma_load_4d(cb ? sV1(st) : sV(st), &kv_map, cb * 64, head, start, 2 * cd.page + 1, v_full(st));
         }
         ++issued;
+        if (!v_ok) {  // this chunk's K is in flight (the drain waits for it), its V is not
+          k_only_last = true;
+          signal_abort(p.status, abort_flag);
+          break;
+        }
       }
-      for (int i = issued > S ? issued - S : 0; i < issued; ++i)  // drain: copies must land before exit
+      // drain: copies must land before exit
+      for (int i = issued > S ? issued - S : 0; i < issued; ++i) {
         ptx::mbar_wait_bounded(full_bar(i % S), (i / S) & 1, limit, nullptr);
+        if (kSplitKV && !(k_only_last && i == issued - 1))
+          ptx::mbar_wait_bounded(v_full(i % S), (i / S) & 1, limit, nullptr);
+      }
     } else if (kDiag && lane == 1 && p.trace != nullptr && blockIdx.x == 0) {
       // trace mode: watch the full barriers and record when each chunk's K/V lands
       for (int i = 0; i < n; ++i)
@@ -578,14 +607,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ptx::mma_commit(s_full(t, kEarly ? 0 : (g & 1)));
+          if (kSplitKV && (g & 1)) ptx::mma_commit(empty_bar(st));  // the chunk's K is read
           if (t == 0) trace<kDiag>(p, (g & 1) ? kTrQk0h1 : kTrQk0, c);
           else if ((g & 1) == 0) trace<kDiag>(p, kTrQk1, c);
           return true;
         };
         // O_t (+)= P V over the 64 keys of half g: a k-step is 16 key rows (2 KB) of V and 8
         // TMEM columns of packed P
-        auto issue_pv = [&](int g) {
+        auto issue_pv = [&](int g) -> bool {
           const int b = g & 1, c = g >> 1, st = c % S;
+          if (kSplitKV && b == 0) {
+            if (!ptx::mbar_wait_bounded(v_full(st), (c / S) & 1, limit, abort_flag)) return false;
+            ptx::tc_fence_after();
+          }
           const uint32_t v_lo = v_lo_of(st) + uint32_t(b) * kHalfRows;
           const uint32_t tP = tmem + p_col<D>(t, b);
 #pragma unroll
@@ -593,9 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_ts_lh(tO, tP + 8 * k, v_lo + uint32_t(128 * k), hi, idesc_pv, (g > 0 || k > 0) ? 1u : 0u);
           ptx::mma_commit(pv_done(t));
           if (b) {
-            ptx::mma_commit(empty_bar(st));  // this consumer is done with the stage
+            ptx::mma_commit(v_empty(st));  // this consumer is done with the stage (its V)
             if (t == 0) trace<kDiag>(p, kTrEmpty, c);
           }
+          return true;
         };
         auto wait_p = [&](int g) -> bool {
           const int b = g & 1, c = g >> 1;
@@ -617,14 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (dump) continue;
             if (!(ok = wait_p(g))) break;
-            issue_pv(g);
+            if (!(ok = issue_pv(g))) break;
           }
         } else {
           // two S buffers: Q K^T of half g+2 into the buffer the PV of half g reads (in order)
           for (int g = 0; ok && g < min(halves, 2); ++g) ok = issue_qk(g);
           for (int g = 0; ok && !dump && g < halves; ++g) {
             if (!(ok = wait_p(g))) break;
-            issue_pv(g);
+            if (!(ok = issue_pv(g))) break;
             if (g + 2 < halves) ok = issue_qk(g + 2);
           }
         }
@@ -653,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else ptx::mma_ss_lh<1>(tS2, k_lo + aoff, q2_lo + boff, hi, idesc_st);
           }
           ptx::mma_commit(s2_full);
+          if (kSplitKV) ptx::mma_commit(empty_bar(st));  // the tail is done with the chunk's K
           trace<kDiag>(p, kTrQk2, c);
           return true;
         };
@@ -668,6 +704,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = ptx::mbar_wait_bounded(p2_ready(c & 1), (c >> 1) & 1, limit, abort_flag))) break;
           ptx::tc_fence_after();
           trace<kDiag>(p, kTrP2Seen, c);
+          if (kSplitKV) {
+            if (!(ok = ptx::mbar_wait_bounded(v_full(st), (c / S) & 1, limit, abort_flag))) break;
+            ptx::tc_fence_after();
+          }
           const uint32_t v_lo = v_lo_of(st);
           const uint32_t b_lo = p2_lo + uint32_t((c & 1) * (C::kP2Bytes >> 4));
 #pragma unroll
@@ -677,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else ptx::mma_ss_lh<1>(tO2, v_lo + uint32_t(128 * k), b_lo + boff, hi, idesc_pv);
           }
           ptx::mma_commit(pv2_done);
-          ptx::mma_commit(empty_bar(st));
+          ptx::mma_commit(v_empty(st));
         }
       }
       if (!ok) signal_abort(p.status, abort_flag);
@@ -820,7 +860,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (len < kHalfKeys * (b + 1)) {
           // ragged chunk: zero this half's V rows past the valid keys before the PV reads them
-          zero_v_rows<D>(sV((g >> 1) % S), sV1((g >> 1) % S), max(len, kHalfKeys * b), kHalfKeys * (b + 1), r, 128);
+          // (head_dim 128: once the chunk's V, which lands apart from K, is there)
+          const int c = g >> 1;
+          if (kSplitKV && !(ok = ptx::mbar_wait_warp(v_full(c % S), (c / S) & 1, limit, abort_flag))) break;
+          zero_v_rows<D>(sV(c % S), sV1(c % S), max(len, kHalfKeys * b), kHalfKeys * (b + 1), r, 128);
           ptx::fence_proxy_async_smem();
         }
         ptx::tc_fence_before();
@@ -970,7 +1013,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_u16(p2_addr(p2, C::kP2ColBlock, rr, key), __bfloat16_as_ushort(pb));
           }
         }
-        if (len < kChunkTokens) zero_v_rows<D>(sV(j % S), sV1(j % S), len, kChunkTokens, tid, 128);
+        if (len < kChunkTokens) {
+          // head_dim 128: the chunk's V lands apart from K; a failed wait skips the zeroing
+          // and is reported at the next chunk's exchange (or after the loop)
+          if (!kSplitKV || ptx::mbar_wait_warp(v_full(j % S), (j / S) & 1, limit, abort_flag))
+            zero_v_rows<D>(sV(j % S), sV1(j % S), len, kChunkTokens, tid, 128);
+          else
+            ok = false;
+        }
         ptx::fence_proxy_async_smem();  // P2 stores (and zeroed V rows) -> visible to the tensor core
         ptx::tc_fence_before();
         long long t_arrive = 0;
